@@ -1,0 +1,209 @@
+/*
+ * oomb.h -- C ABI of the paged sparse chunk-attention library (liboomb.so).
+ *
+ * The operations are those of OOMB's chunk-recurrent long-context training
+ * ("Out of the Memory Barrier: A Highly Memory Efficient Training System for LLMs
+ * with Million-Token Contexts"; gist.science explainer, section 2 "Methodology"):
+ * one query chunk attends, causally and with grouped KV heads, to the keys of a
+ * paged KV cache that holds every earlier chunk, restricted to the top-K pages
+ * chosen by a mean-key page summary plus the sink page and the chunk's own pages;
+ * the backward pass recomputes the attention probabilities, writes dQ and adds
+ * dK/dV in place into a paged fp32 gradient pool that shares the KV page table.
+ *
+ * Conventions shared by every call
+ *  - Ownership: the caller allocates and owns every buffer named in
+ *    oomb_pool_desc and every argument pointer.  The library owns only the opaque
+ *    oomb_pool object (host memory: free list and a host copy of the page table).
+ *    No call allocates device memory.
+ *  - Streams: `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Every call is stream-ordered and asynchronous unless stated.
+ *  - Errors: every call checks its arguments on the host and returns a status;
+ *    nothing aborts, throws across the ABI or traps on the device.  Kernels that
+ *    meet a bad page-table entry or selection index, or whose bounded waits run
+ *    out, set bits in the caller's device error word and skip the access;
+ *    oomb_check() reads and clears that word.
+ *  - Layouts (row-major, innermost last):
+ *      K/V of a chunk      [n_tokens, Hkv, d]        (token-major, dtype)
+ *      Q, O, dO, dQ        [n_q, Hq, d]              (token-major, dtype)
+ *      LSE                 [Hq, n_q] fp32            (natural log)
+ *      K/V pools           [num_phys, Hkv, P, d]     (dtype)
+ *      dK/dV pools         [num_phys, Hkv, P, d]     fp32
+ *      page summary        [num_phys, Hkv, d]        fp32 (mean key)
+ *      page table          [max_logical_pages] int32 (logical -> physical, -1 unmapped)
+ *      selection           sel [Hkv, max_sel] int32 (logical pages, ascending),
+ *                          sel_count [Hkv] int32
+ *    Query head hq uses KV head hq / (Hq / Hkv).
+ *  - Alignment: every pointer 16-byte aligned; pools 1024-byte aligned for the
+ *    bf16 tensor-core path.  Appends start on a page boundary.
+ *  - Supported shapes: fp32 with head_dim <= 128 (multiple of 4), any page size
+ *    up to 256; bf16 with head_dim <= 128 (multiple of 8).  bf16 with head_dim 128
+ *    and page size 128 runs on the tcgen05 tensor-core kernels; other bf16 shapes
+ *    on the SIMT kernels.
+ *  - Thread safety: one pool must not be used from two host threads at once.
+ */
+#ifndef OOMB_H
+#define OOMB_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define OOMB_API __attribute__((visibility("default")))
+#else
+#define OOMB_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  OOMB_OK = 0,
+  OOMB_ERR_ARG = 1,          /* bad argument (null pointer, size, shape) */
+  OOMB_ERR_OUT_OF_PAGES = 2, /* the free list cannot cover the append */
+  OOMB_ERR_ALIGN = 3,        /* pointer or token offset misaligned */
+  OOMB_ERR_DTYPE = 4,        /* unknown dtype */
+  OOMB_ERR_KERNEL = 5,       /* a kernel raised the device error word */
+  OOMB_ERR_TIMEOUT = 6,      /* a bounded device wait gave up */
+  OOMB_ERR_CUDA = 7,         /* a CUDA runtime call failed */
+  OOMB_ERR_UNSUPPORTED = 8,  /* valid but not implemented (shape/dtype/device) */
+  OOMB_ERR_WORKSPACE = 9     /* workspace missing or too small */
+} oomb_status;
+
+typedef enum { OOMB_BF16 = 0, OOMB_FP32 = 1 } oomb_dtype;
+
+/* Operation selector for oomb_workspace_size. */
+typedef enum { OOMB_OP_SELECT = 0, OOMB_OP_BWD = 1 } oomb_op;
+
+/* Device error-word bits (see oomb_check). */
+#define OOMB_DEVERR_TIMEOUT 0x1u  /* an mbarrier wait ran out */
+#define OOMB_DEVERR_PAGE 0x2u     /* page table entry unmapped / out of range */
+#define OOMB_DEVERR_SEL 0x4u      /* selection index out of range */
+#define OOMB_DEVERR_TMEM 0x8u     /* tensor-memory allocation failed */
+
+typedef struct {
+  int n_q_heads;         /* Hq */
+  int n_kv_heads;        /* Hkv; Hq % Hkv == 0 */
+  int head_dim;          /* d */
+  int page_size;         /* P, tokens per page */
+  int num_phys_pages;    /* pages in each pool */
+  int max_logical_pages; /* entries of page_table */
+  int dtype;             /* oomb_dtype of K/V pools, Q, O, dO, dQ */
+  void* k_pool;          /* [num_phys, Hkv, P, d]; device, or pinned+mapped host if offload */
+  void* v_pool;          /* same */
+  float* dk_pool;        /* [num_phys, Hkv, P, d] fp32 device */
+  float* dv_pool;        /* same */
+  float* summary;        /* [num_phys, Hkv, d] fp32 device */
+  int32_t* page_table;   /* [max_logical_pages] device; written by the library */
+  uint32_t* error_word;  /* one device uint32, zero at creation */
+  const int32_t* page_order; /* optional host [num_phys]: order in which physical
+                                pages are handed out (copied at creation); NULL = 0..n-1 */
+  int offload;           /* 1: k_pool/v_pool live in pinned host memory and the
+                            attention kernels read selected pages from staging */
+  void* stage_k;         /* offload only: [2, Hkv, stage_max_sel, P, d] device */
+  void* stage_v;         /* same */
+  int stage_max_sel;     /* offload only: selection capacity per KV head */
+} oomb_pool_desc;
+
+typedef struct oomb_pool oomb_pool;
+
+/* Validate `desc`, copy it and build the free list.  Touches no device memory:
+ * the page table is filled with -1 on the stream of the first append (or
+ * reset).  On success *out owns a host object that oomb_pool_destroy frees. */
+OOMB_API oomb_status oomb_pool_create(const oomb_pool_desc* desc, oomb_pool** out);
+OOMB_API void oomb_pool_destroy(oomb_pool* pool);
+
+/* Return every page to the free list, in the creation order, and set every
+ * page-table entry to -1 (stream-ordered).  The pools' contents are kept. */
+OOMB_API oomb_status oomb_pool_reset(oomb_pool* pool, void* stream);
+
+/* Paged KV append (explainer 2.B "Paged KV Cache and Gradient Management"; the
+ * lay summary's "Trick A": each chunk's KV drops onto the next free page, no
+ * copying of earlier pages).  Opens ceil((first_token+n)/P) - first_token/P new
+ * logical pages, taking physical pages from the free list and writing their
+ * page-table entries; copies k, v ([n_tokens, Hkv, d], dtype, device) into the
+ * pools; zeroes the dK/dV rows of the written tokens; writes the page summary
+ * (fp32 mean key over the tokens present) of every touched page.
+ * first_token must equal the tokens already appended and be a multiple of P.
+ * Errors: ARG, ALIGN, OUT_OF_PAGES (nothing is written), CUDA. */
+OOMB_API oomb_status oomb_kv_append(oomb_pool* pool, const void* k, const void* v, int64_t first_token, int n_tokens,
+                           void* stream);
+
+/* Page selection for one query chunk (explainer 2.D "Page-Level Sparse
+ * Attention": top-K pages by a representative, averaged key).  With
+ * qbar_h = mean of q over the chunk's n_q tokens and the G query heads of KV
+ * head h, every complete history page p in [n_sink, q_start/P) is scored as
+ * qbar_h . summary[phi(p), h]; the top_k highest scores are kept (ties to the
+ * lower logical page), plus pages [0, n_sink) and the chunk's own pages
+ * [q_start/P, ceil((q_start+n_q)/P)).  top_k < 0 keeps every page.
+ * Output per KV head: ascending logical pages in sel[h*max_sel ...], count in
+ * sel_count[h].  q: [n_q, Hq, d] device.  q_start must be a multiple of P and
+ * the chunk's own K/V already appended.  Workspace: oomb_workspace_size(
+ * OOMB_OP_SELECT, n_q) bytes of device memory, contents scratch.
+ * Errors: ARG (incl. max_sel too small), ALIGN, WORKSPACE, CUDA. */
+OOMB_API oomb_status oomb_page_select(oomb_pool* pool, const void* q, int64_t q_start, int n_q, int top_k, int n_sink,
+                             int32_t* sel, int32_t* sel_count, int max_sel, void* workspace, size_t ws_bytes,
+                             void* stream);
+
+/* Chunk attention forward.  For query head hq and row i (absolute position
+ * q_start+i): keys = every token of the selected pages of KV head hq/G with
+ * position <= q_start+i; O_i = softmax(scale * q_i . k_j) V and
+ * LSE_i = log sum_j exp(scale * q_i . k_j).  q/o: [n_q, Hq, d] device,
+ * lse: [Hq, n_q] fp32 device.  sel/sel_count as written by oomb_page_select
+ * (device).  In offload mode K/V are read from staging buffer
+ * oomb_pool_set_stage(); the selection must equal the one prefetched.
+ * Errors: ARG, ALIGN, UNSUPPORTED, CUDA. */
+OOMB_API oomb_status oomb_chunk_attn_fwd(oomb_pool* pool, const void* q, int64_t q_start, int n_q, const int32_t* sel,
+                                const int32_t* sel_count, int max_sel, float softmax_scale, void* o, float* lse,
+                                void* stream);
+
+/* Chunk attention backward with on-the-fly recomputation (explainer 2.A) and
+ * in-place paged gradient accumulation (explainer 2.B).  With
+ * P_ij = exp(scale q_i.k_j - LSE_i) over the forward's key set,
+ * dP = dO V^T, D_i = dO_i . O_i, dS = P (dP - D):
+ *   dq = scale dS K (written, dtype),
+ *   dK_pool[phi(p), h] += scale dS^T Q,  dV_pool[phi(p), h] += P^T dO
+ * summed over the G query heads of KV head h and every row of the chunk.
+ * Each (page, KV head) block of the gradient pool is updated by exactly one
+ * thread block: no global atomics on dK/dV.
+ * Workspace: oomb_workspace_size(OOMB_OP_BWD, n_q) bytes, contents scratch.
+ * Errors: ARG, ALIGN, WORKSPACE, UNSUPPORTED, CUDA. */
+OOMB_API oomb_status oomb_chunk_attn_bwd(oomb_pool* pool, const void* q, const void* o, const void* d_o, const float* lse,
+                                int64_t q_start, int n_q, const int32_t* sel, const int32_t* sel_count, int max_sel,
+                                float softmax_scale, void* dq, void* workspace, size_t ws_bytes, void* stream);
+
+/* Offload mode (explainer 2.C "Asynchronous KV Cache CPU Offloading"): copy the
+ * selected (page, KV head) blocks of K and V from the pinned host pools into
+ * staging buffer `stage_buf` (0 or 1) on `stream` (normally a side stream;
+ * order it against the attention calls with CUDA events).  Block s of KV head h
+ * lands in slot (stage_buf, h, s).  Errors: ARG, UNSUPPORTED (pool not in
+ * offload mode), CUDA. */
+OOMB_API oomb_status oomb_prefetch(oomb_pool* pool, const int32_t* sel, const int32_t* sel_count, int max_sel,
+                          int stage_buf, void* stream);
+
+/* Offload mode: staging buffer that following attention calls read. */
+OOMB_API oomb_status oomb_pool_set_stage(oomb_pool* pool, int stage_buf);
+
+/* Bytes of device workspace `op` needs for a chunk of n_q queries (0 on error). */
+OOMB_API size_t oomb_workspace_size(const oomb_pool* pool, int op, int n_q);
+
+/* Synchronize `stream`, read and clear the device error word.  Returns OK,
+ * KERNEL (bits in *bits_out if non-NULL) or CUDA. */
+OOMB_API oomb_status oomb_check(oomb_pool* pool, void* stream, uint32_t* bits_out);
+
+/* Host copy of the page table (n entries from logical page 0). Returns entries copied. */
+OOMB_API int oomb_page_table_host(const oomb_pool* pool, int32_t* out, int n);
+
+/* Tokens appended so far and free pages left. */
+OOMB_API int64_t oomb_pool_tokens(const oomb_pool* pool);
+OOMB_API int oomb_pool_free_pages(const oomb_pool* pool);
+
+OOMB_API const char* oomb_status_str(oomb_status s);
+
+/* Which attention kernels a call with this pool would use: 1 = tcgen05, 0 = SIMT. */
+OOMB_API int oomb_uses_tensor_cores(const oomb_pool* pool);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* OOMB_H */

@@ -1,0 +1,185 @@
+"""ctypes binding of liboomb.so: argument marshalling only.
+
+Every function here forwards to the C entry point of the same name in
+include/oomb.h, passing raw device pointers taken from torch tensors.  There is
+no fallback: if liboomb.so is missing the import of the binding fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import re
+from typing import Optional
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "liboomb.so")
+HEADER = os.path.join(os.path.dirname(PKG), "include", "oomb.h")
+
+OOMB_BF16, OOMB_FP32 = 0, 1
+OOMB_OP_SELECT, OOMB_OP_BWD = 0, 1
+STATUS = {0: "OK", 1: "ERR_ARG", 2: "ERR_OUT_OF_PAGES", 3: "ERR_ALIGN", 4: "ERR_DTYPE", 5: "ERR_KERNEL",
+          6: "ERR_TIMEOUT", 7: "ERR_CUDA", 8: "ERR_UNSUPPORTED", 9: "ERR_WORKSPACE"}
+
+
+class OombError(RuntimeError):
+    def __init__(self, func: str, status: int, detail: str = ""):
+        self.status = status
+        super().__init__(f"{func}: {STATUS.get(status, status)} ({detail})")
+
+
+class PoolDesc(C.Structure):
+    _fields_ = [
+        ("n_q_heads", C.c_int), ("n_kv_heads", C.c_int), ("head_dim", C.c_int), ("page_size", C.c_int),
+        ("num_phys_pages", C.c_int), ("max_logical_pages", C.c_int), ("dtype", C.c_int),
+        ("k_pool", C.c_void_p), ("v_pool", C.c_void_p), ("dk_pool", C.c_void_p), ("dv_pool", C.c_void_p),
+        ("summary", C.c_void_p), ("page_table", C.c_void_p), ("error_word", C.c_void_p),
+        ("page_order", C.c_void_p), ("offload", C.c_int), ("stage_k", C.c_void_p), ("stage_v", C.c_void_p),
+        ("stage_max_sel", C.c_int),
+    ]
+
+
+_lib: Optional[C.CDLL] = None
+
+
+def header_symbols():
+    """Names of the entry points include/oomb.h declares."""
+    with open(HEADER) as f:
+        txt = f.read()
+    return sorted(set(re.findall(r"OOMB_API\s+[\w\s\*]+?\b(oomb_\w+)\s*\(", txt)))
+
+
+def load(path: str = LIB_PATH) -> C.CDLL:
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is not built: run __graft_entry__.build() (nvcc, sm_103a)")
+    lib = C.CDLL(path)
+    vp, i32, i64, f32, sz = C.c_void_p, C.c_int, C.c_int64, C.c_float, C.c_size_t
+    sig = {
+        "oomb_pool_create": (i32, [C.POINTER(PoolDesc), C.POINTER(vp)]),
+        "oomb_pool_destroy": (None, [vp]),
+        "oomb_pool_reset": (i32, [vp, vp]),
+        "oomb_kv_append": (i32, [vp, vp, vp, i64, i32, vp]),
+        "oomb_page_select": (i32, [vp, vp, i64, i32, i32, i32, vp, vp, i32, vp, sz, vp]),
+        "oomb_chunk_attn_fwd": (i32, [vp, vp, i64, i32, vp, vp, i32, f32, vp, vp, vp]),
+        "oomb_chunk_attn_bwd": (i32, [vp, vp, vp, vp, vp, i64, i32, vp, vp, i32, f32, vp, vp, sz, vp]),
+        "oomb_prefetch": (i32, [vp, vp, vp, i32, i32, vp]),
+        "oomb_pool_set_stage": (i32, [vp, i32]),
+        "oomb_workspace_size": (sz, [vp, i32, i32]),
+        "oomb_check": (i32, [vp, vp, C.POINTER(C.c_uint32)]),
+        "oomb_page_table_host": (i32, [vp, vp, i32]),
+        "oomb_pool_tokens": (i64, [vp]),
+        "oomb_pool_free_pages": (i32, [vp]),
+        "oomb_status_str": (C.c_char_p, [i32]),
+        "oomb_uses_tensor_cores": (i32, [vp]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    return t.data_ptr() if hasattr(t, "data_ptr") else int(t)
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ok(name: str, st: int):
+    if st != 0:
+        raise OombError(name, st, load().oomb_status_str(st).decode())
+
+
+# ---------------------------------------------------------------- entry points
+def oomb_pool_create(desc: PoolDesc) -> int:
+    h = C.c_void_p()
+    _ok("oomb_pool_create", load().oomb_pool_create(C.byref(desc), C.byref(h)))
+    return h.value
+
+
+def oomb_pool_destroy(pool: int) -> None:
+    load().oomb_pool_destroy(pool)
+
+
+def oomb_pool_reset(pool: int, stream=None) -> None:
+    _ok("oomb_pool_reset", load().oomb_pool_reset(pool, _stream(stream)))
+
+
+def oomb_kv_append(pool: int, k, v, first_token: int, n_tokens: Optional[int] = None, stream=None) -> None:
+    n = k.shape[0] if n_tokens is None else n_tokens
+    _ok("oomb_kv_append", load().oomb_kv_append(pool, _ptr(k), _ptr(v), first_token, n, _stream(stream)))
+
+
+def oomb_page_select(pool: int, q, q_start: int, top_k: int, n_sink: int, sel, sel_count, workspace,
+                     n_q: Optional[int] = None, stream=None) -> None:
+    n = q.shape[0] if n_q is None else n_q
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _ok("oomb_page_select", load().oomb_page_select(pool, _ptr(q), q_start, n, top_k, n_sink, _ptr(sel),
+                                                    _ptr(sel_count), sel.shape[-1], _ptr(workspace), ws_bytes,
+                                                    _stream(stream)))
+
+
+def oomb_chunk_attn_fwd(pool: int, q, q_start: int, sel, sel_count, softmax_scale: float, o, lse,
+                        n_q: Optional[int] = None, stream=None) -> None:
+    n = q.shape[0] if n_q is None else n_q
+    _ok("oomb_chunk_attn_fwd", load().oomb_chunk_attn_fwd(pool, _ptr(q), q_start, n, _ptr(sel), _ptr(sel_count),
+                                                          sel.shape[-1], softmax_scale, _ptr(o), _ptr(lse),
+                                                          _stream(stream)))
+
+
+def oomb_chunk_attn_bwd(pool: int, q, o, d_o, lse, q_start: int, sel, sel_count, softmax_scale: float, dq,
+                        workspace, n_q: Optional[int] = None, stream=None) -> None:
+    n = q.shape[0] if n_q is None else n_q
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _ok("oomb_chunk_attn_bwd", load().oomb_chunk_attn_bwd(pool, _ptr(q), _ptr(o), _ptr(d_o), _ptr(lse), q_start, n,
+                                                          _ptr(sel), _ptr(sel_count), sel.shape[-1], softmax_scale,
+                                                          _ptr(dq), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def oomb_prefetch(pool: int, sel, sel_count, stage_buf: int, stream=None) -> None:
+    _ok("oomb_prefetch", load().oomb_prefetch(pool, _ptr(sel), _ptr(sel_count), sel.shape[-1], stage_buf,
+                                              _stream(stream)))
+
+
+def oomb_pool_set_stage(pool: int, stage_buf: int) -> None:
+    _ok("oomb_pool_set_stage", load().oomb_pool_set_stage(pool, stage_buf))
+
+
+def oomb_workspace_size(pool: int, op: int, n_q: int) -> int:
+    return int(load().oomb_workspace_size(pool, op, n_q))
+
+
+def oomb_check(pool: int, stream=None) -> int:
+    bits = C.c_uint32(0)
+    st = load().oomb_check(pool, _stream(stream), C.byref(bits))
+    if st != 0:
+        raise OombError("oomb_check", st, f"device error bits 0x{bits.value:x}")
+    return bits.value
+
+
+def oomb_page_table_host(pool: int, n: int):
+    buf = (C.c_int32 * n)()
+    m = load().oomb_page_table_host(pool, buf, n)
+    return list(buf)[:m]
+
+
+def oomb_pool_tokens(pool: int) -> int:
+    return int(load().oomb_pool_tokens(pool))
+
+
+def oomb_pool_free_pages(pool: int) -> int:
+    return int(load().oomb_pool_free_pages(pool))
+
+
+def oomb_uses_tensor_cores(pool: int) -> bool:
+    return bool(load().oomb_uses_tensor_cores(pool))

@@ -1,0 +1,128 @@
+// Paged KV append with fused page summary and gradient-page zeroing.
+//
+// "Out of the Memory Barrier" (gist.science explainer, 2.B "Paged KV Cache and
+// Gradient Management", and the lay summary's "Trick A"): a chunk's K/V go onto
+// the next free fixed-size pages through the page table, without copying earlier
+// pages; the KV gradients live in pages that share the same table.  The page
+// summary is the representative vector of 2.D, fixed as the mean key per page.
+//
+// One thread block per (new page, KV head, K-or-V).  HBM traffic per token and KV
+// head: read K,V (2 d esize), write K,V (2 d esize), zero dK,dV (2 d 4 bytes);
+// plus one fp32 summary row per page and head.
+#include "oomb_internal.h"
+
+namespace oomb {
+namespace {
+
+constexpr int kAppendThreads = 256;
+constexpr int kMaxNewPerLaunch = 1024;
+
+struct NewPages {
+  int32_t phys[kMaxNewPerLaunch];
+};
+
+template <typename T>
+__device__ __forceinline__ float to_f(T x);
+template <>
+__device__ __forceinline__ float to_f<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T>
+__global__ void __launch_bounds__(kAppendThreads)
+    kv_append_kernel(Geometry g, T* __restrict__ k_pool, T* __restrict__ v_pool, float* __restrict__ dk_pool,
+                     float* __restrict__ dv_pool, float* __restrict__ summary, int32_t* __restrict__ table,
+                     const T* __restrict__ k, const T* __restrict__ v, int64_t first_token, int64_t end_token,
+                     int first_new_logical, const __grid_constant__ NewPages np, int n_new, uint32_t* err) {
+  const int i = blockIdx.x, h = blockIdx.y, which = blockIdx.z;
+  const int P = g.P, d = g.d, Hkv = g.Hkv;
+  const int phys = np.phys[i];
+  if (phys < 0 || phys >= g.num_phys) {
+    if (threadIdx.x == 0) atomicOr(err, OOMB_DEVERR_PAGE);
+    return;
+  }
+  const int64_t logical = (int64_t)first_new_logical + i;
+  if (which == 0 && h == 0 && threadIdx.x == 0) table[logical] = phys;
+  const int64_t t0 = logical * P;
+  const int m = (int)(end_token - t0 < P ? end_token - t0 : P);  // tokens present in this page
+
+  constexpr int VEC = 16 / sizeof(T);
+  const int nvec = d / VEC;  // 16-byte vectors per row
+  const size_t blk = ((size_t)phys * Hkv + h) * (size_t)P * d;
+  const T* src = (which == 0 ? k : v);
+  T* dst = (which == 0 ? k_pool : v_pool) + blk;
+  float* gdst = (which == 0 ? dk_pool : dv_pool) + blk;
+
+  // copy K or V rows (zero the absent tail rows of a partial page)
+  for (int idx = threadIdx.x; idx < P * nvec; idx += kAppendThreads) {
+    const int r = idx / nvec, c = idx % nvec;
+    uint4 val = make_uint4(0, 0, 0, 0);
+    if (r < m) {
+      const int64_t tok = t0 + r - first_token;
+      val = *reinterpret_cast<const uint4*>(src + ((size_t)tok * Hkv + h) * d + (size_t)c * VEC);
+    }
+    *reinterpret_cast<uint4*>(dst + (size_t)r * d + (size_t)c * VEC) = val;
+  }
+  // zero the gradient page
+  const int nvec4 = d / 4;
+  for (int idx = threadIdx.x; idx < P * nvec4; idx += kAppendThreads)
+    reinterpret_cast<float4*>(gdst)[idx] = make_float4(0.f, 0.f, 0.f, 0.f);
+
+  if (which != 0) return;
+  // mean key over the m tokens present: fixed-order reduction, deterministic.
+  __shared__ float part[kAppendThreads * VEC];
+  const int n_rg = kAppendThreads / nvec;
+  const int c = threadIdx.x % nvec, rg = threadIdx.x / nvec;
+  float acc[VEC];
+#pragma unroll
+  for (int e = 0; e < VEC; ++e) acc[e] = 0.f;
+  if (rg < n_rg) {
+    for (int r = rg; r < m; r += n_rg) {
+      const int64_t tok = t0 + r - first_token;
+      const T* row = src + ((size_t)tok * Hkv + h) * d + (size_t)c * VEC;
+      uint4 raw = *reinterpret_cast<const uint4*>(row);
+      const T* x = reinterpret_cast<const T*>(&raw);
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) acc[e] += to_f<T>(x[e]);
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < VEC; ++e) part[threadIdx.x * VEC + e] = acc[e];
+  __syncthreads();
+  for (int col = threadIdx.x; col < d; col += kAppendThreads) {
+    const int cc = col / VEC, e = col % VEC;
+    float s = 0.f;
+    for (int r = 0; r < n_rg; ++r) s += part[(r * nvec + cc) * VEC + e];
+    summary[((size_t)phys * Hkv + h) * d + col] = s / (float)m;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_kv_append(const Geometry& g, void* k_pool, void* v_pool, float* dk_pool, float* dv_pool,
+                             float* summary, int32_t* table, const void* k, const void* v, int64_t first_token,
+                             int n_tokens, int64_t total_tokens, const int32_t* new_phys, int n_new,
+                             int first_new_logical, uint32_t* err, cudaStream_t st) {
+  (void)n_tokens;
+  for (int base = 0; base < n_new; base += kMaxNewPerLaunch) {
+    const int cnt = n_new - base < kMaxNewPerLaunch ? n_new - base : kMaxNewPerLaunch;
+    NewPages np;
+    for (int i = 0; i < cnt; ++i) np.phys[i] = new_phys[base + i];
+    dim3 grid(cnt, g.Hkv, 2);
+    if (g.dtype == OOMB_FP32) {
+      kv_append_kernel<float><<<grid, kAppendThreads, 0, st>>>(
+          g, (float*)k_pool, (float*)v_pool, dk_pool, dv_pool, summary, table, (const float*)k, (const float*)v,
+          first_token, total_tokens, first_new_logical + base, np, cnt, err);
+    } else {
+      kv_append_kernel<__nv_bfloat16><<<grid, kAppendThreads, 0, st>>>(
+          g, (__nv_bfloat16*)k_pool, (__nv_bfloat16*)v_pool, dk_pool, dv_pool, summary, table,
+          (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, first_token, total_tokens, first_new_logical + base,
+          np, cnt, err);
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace oomb

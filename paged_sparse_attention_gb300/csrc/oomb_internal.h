@@ -1,0 +1,79 @@
+// Internal declarations shared by the C-ABI layer and the kernel translation units.
+#pragma once
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+#include <vector>
+
+#include "../../include/oomb.h"
+
+namespace oomb {
+
+// Where a chunk's K/V blocks are read from.
+//  resident: block(p, h) = table[p] * Hkv + h          in k/v
+//  staged:   block(s, h) = (stage_base + h) * stride + s  in k/v (= staging buffers)
+struct KvSource {
+  const void* k;
+  const void* v;
+  const int32_t* table;  // logical -> physical page (resident mode and dK/dV addressing)
+  int staged;            // 1: read K/V from staging slots
+  int stage_h0;          // buffer index * Hkv
+  int stage_stride;      // stage_max_sel
+};
+
+struct Geometry {
+  int Hq, Hkv, G, d, P;
+  int num_phys;
+  int max_logical;
+  int dtype;  // oomb_dtype
+};
+
+struct AttnArgs {
+  Geometry g;
+  KvSource kv;
+  const void* q;
+  const void* o;
+  const void* dout;
+  const float* lse_in;
+  float* lse_out;
+  void* o_out;
+  void* dq;
+  float* dk_pool;
+  float* dv_pool;
+  const int32_t* sel;
+  const int32_t* sel_count;
+  int max_sel;
+  int64_t q_start;
+  int n_q;
+  float scale;
+  uint32_t* err;
+  void* ws;  // backward workspace
+  size_t ws_bytes;
+};
+
+// ---- launchers (return cudaGetLastError of the launch) ----
+cudaError_t launch_kv_append(const Geometry& g, void* k_pool, void* v_pool, float* dk_pool, float* dv_pool,
+                             float* summary, int32_t* table, const void* k, const void* v, int64_t first_token,
+                             int n_tokens, int64_t total_tokens, const int32_t* new_phys, int n_new,
+                             int first_new_logical, uint32_t* err, cudaStream_t st);
+
+size_t select_workspace_bytes(const Geometry& g, int n_q);
+cudaError_t launch_page_select(const Geometry& g, const float* summary, const int32_t* table, const void* q,
+                               int64_t q_start, int n_q, int top_k, int n_sink, int32_t* sel, int32_t* sel_count,
+                               int max_sel, void* ws, uint32_t* err, cudaStream_t st);
+
+size_t bwd_workspace_bytes(const Geometry& g, int n_q);
+cudaError_t launch_attn_fwd_simt(const AttnArgs& a, cudaStream_t st);
+cudaError_t launch_attn_bwd_simt(const AttnArgs& a, cudaStream_t st);
+bool tc_supported(const Geometry& g);
+cudaError_t launch_attn_fwd_tc(const AttnArgs& a, cudaStream_t st);
+cudaError_t launch_attn_bwd_tc(const AttnArgs& a, cudaStream_t st);
+
+cudaError_t launch_prefetch(const Geometry& g, const void* k_pool, const void* v_pool, const int32_t* table,
+                            const int32_t* sel, const int32_t* sel_count, int max_sel, void* stage_k, void* stage_v,
+                            int stage_h0, int stage_stride, uint32_t* err, cudaStream_t st);
+
+__host__ __device__ inline size_t dtype_size(int dt) { return dt == OOMB_FP32 ? 4 : 2; }
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace oomb

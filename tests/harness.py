@@ -1,0 +1,108 @@
+"""Shared helpers for the GPU parity tests: run a workload through the C ABI and
+through the fp64 oracle on the same seeded inputs."""
+from __future__ import annotations
+
+import math
+from typing import List, Optional
+
+import numpy as np
+import torch
+
+import oracle.oomb_oracle as O
+import paged_sparse_attention_gb300 as L
+from paged_sparse_attention_gb300 import synth
+from paged_sparse_attention_gb300.pool import PagedKVPool
+
+TOL = {"fp32": 1e-5, "bf16": 1e-2}
+
+
+def f64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().double().cpu().numpy()
+
+
+def make_chunks(w: synth.Workload, plants: bool = True):
+    pt = synth.PlantTable(w) if (plants and w.plants > 0) else None
+    return [synth.make_chunk(w, c, plants=pt) for c in range(w.n_chunks)], pt
+
+
+def oracle_sweep(w: synth.Workload, chunks, order, scale: Optional[float] = None):
+    scale = 1.0 / math.sqrt(w.head_dim) if scale is None else scale
+    return O.chunked_sweep([{k: v.double().numpy() for k, v in ch.items()} for ch in chunks], list(order),
+                           w.n_kv_heads, w.page, len(order), scale, w.top_k, w.n_sink)
+
+
+def pad_sel(sel_list: List[np.ndarray], max_sel: int, dev):
+    Hkv = len(sel_list)
+    sel = torch.full((Hkv, max_sel), -1, dtype=torch.int32)
+    cnt = torch.zeros(Hkv, dtype=torch.int32)
+    for h, s in enumerate(sel_list):
+        sel[h, : len(s)] = torch.from_numpy(np.asarray(s, dtype=np.int32))
+        cnt[h] = len(s)
+    return sel.to(dev), cnt.to(dev)
+
+
+class GpuSweep:
+    """Forward sweep (append, select, forward) then reverse sweep (recompute
+    forward, backward) through the C ABI.  ``sel_override`` feeds given
+    selections to the attention calls (the GPU selection is still computed and
+    kept in ``gpu_sel``)."""
+
+    def __init__(self, w: synth.Workload, chunks, order, dev="cuda", sel_override=None, scale=None,
+                 num_phys: Optional[int] = None):
+        self.w = w
+        self.dev = torch.device(dev)
+        self.scale = 1.0 / math.sqrt(w.head_dim) if scale is None else scale
+        n_phys = len(order) if num_phys is None else num_phys
+        self.pool = PagedKVPool(w.n_q_heads, w.n_kv_heads, w.head_dim, w.page, n_phys, w.n_pages,
+                                w.torch_dtype, self.dev, page_order=torch.as_tensor(order, dtype=torch.int32))
+        max_sel = w.max_sel if sel_override is None else max(w.max_sel, max(max(len(s) for s in so)
+                                                                               for so in sel_override))
+        self.max_sel = max_sel
+        ws_sel = self.pool.workspace(L.OOMB_OP_SELECT, w.chunk)
+        ws_bwd = self.pool.workspace(L.OOMB_OP_BWD, w.chunk)
+        h = self.pool.handle
+        self.gpu_sel, self.O, self.LSE, self.dQ, self.O2, self.LSE2 = [], [], [], [], [], []
+        dev_chunks = []
+        for c, ch in enumerate(chunks):
+            start, n = w.chunk_bounds(c)
+            g = {k: v.to(self.dev) for k, v in ch.items()}
+            dev_chunks.append(g)
+            L.oomb_kv_append(h, g["k"], g["v"], start)
+            sel = torch.full((w.n_kv_heads, max_sel), -1, dtype=torch.int32, device=self.dev)
+            cnt = torch.zeros(w.n_kv_heads, dtype=torch.int32, device=self.dev)
+            L.oomb_page_select(h, g["q"], start, w.top_k, w.n_sink, sel, cnt, ws_sel)
+            self.gpu_sel.append([sel[i, : int(cnt[i])].cpu().numpy() for i in range(w.n_kv_heads)])
+            if sel_override is not None:
+                sel, cnt = pad_sel(sel_override[c], max_sel, self.dev)
+            o = torch.empty_like(g["q"])
+            lse = torch.empty(w.n_q_heads, n, dtype=torch.float32, device=self.dev)
+            L.oomb_chunk_attn_fwd(h, g["q"], start, sel, cnt, self.scale, o, lse)
+            self.O.append(o)
+            self.LSE.append(lse)
+            g["sel"], g["cnt"] = sel, cnt
+        self.dQ = [None] * len(chunks)
+        for c in range(len(chunks) - 1, -1, -1):
+            start, n = w.chunk_bounds(c)
+            g = dev_chunks[c]
+            o = torch.empty_like(g["q"])
+            lse = torch.empty(w.n_q_heads, n, dtype=torch.float32, device=self.dev)
+            L.oomb_chunk_attn_fwd(h, g["q"], start, g["sel"], g["cnt"], self.scale, o, lse)  # recompute
+            dq = torch.empty_like(g["q"])
+            L.oomb_chunk_attn_bwd(h, g["q"], o, g["do"], lse, start, g["sel"], g["cnt"], self.scale, dq, ws_bwd)
+            self.dQ[c] = dq
+            self.O2.insert(0, o)
+            self.LSE2.insert(0, lse)
+        self.err_bits = L.oomb_check(h)
+        self.dK, self.dV = self.pool.logical_grads(w.seq)
+
+
+def selection_matches(w, gpu_sel, ref_pool_state, q64, start, ora_sel):
+    """GPU and oracle selections agree up to near-ties (relative gap < 1e-4)."""
+    cand, scores = ref_pool_state
+    swaps = 0
+    for h in range(w.n_kv_heads):
+        ok, n = O.near_tie_ok(gpu_sel[h], ora_sel[h], cand, scores[h], w.top_k)
+        if not ok:
+            return False, h
+        swaps += n
+    return True, swaps

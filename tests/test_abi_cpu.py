@@ -1,0 +1,80 @@
+"""CPU-only checks of the C ABI: the library builds, loads, exports every symbol
+include/oomb.h declares, and its host-side argument checks and page allocator
+answer without touching a GPU (pointers below are never dereferenced)."""
+import ctypes as C
+
+import pytest
+
+import paged_sparse_attention_gb300 as L
+from paged_sparse_attention_gb300 import _lib, build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return L.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = L.header_symbols()
+    assert len(names) >= 16
+    for n in ["oomb_kv_append", "oomb_page_select", "oomb_chunk_attn_fwd", "oomb_chunk_attn_bwd",
+              "oomb_prefetch"]:
+        assert n in names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for s in range(10):
+        assert lib.oomb_status_str(s)
+    assert lib.oomb_status_str(2) == b"out of pages"
+
+
+def _desc(**kw):
+    d = _lib.PoolDesc()
+    d.n_q_heads, d.n_kv_heads, d.head_dim, d.page_size = 28, 4, 128, 128
+    d.num_phys_pages, d.max_logical_pages, d.dtype = 4, 8, _lib.OOMB_BF16
+    fake = 1 << 20
+    for i, f in enumerate(["k_pool", "v_pool", "dk_pool", "dv_pool", "summary", "page_table", "error_word"]):
+        setattr(d, f, fake * (i + 1))
+    for k, v in kw.items():
+        setattr(d, k, v)
+    return d
+
+
+def test_pool_create_validation(lib):
+    h = C.c_void_p()
+    assert lib.oomb_pool_create(C.byref(_desc(dtype=7)), C.byref(h)) == 4
+    assert lib.oomb_pool_create(C.byref(_desc(n_kv_heads=3)), C.byref(h)) == 1
+    assert lib.oomb_pool_create(C.byref(_desc(head_dim=256)), C.byref(h)) == 8
+    assert lib.oomb_pool_create(C.byref(_desc(k_pool=(1 << 20) + 4)), C.byref(h)) == 3
+    assert lib.oomb_pool_create(C.byref(_desc(summary=None)), C.byref(h)) == 1
+    bad_order = (C.c_int32 * 4)(0, 1, 1, 2)
+    assert lib.oomb_pool_create(C.byref(_desc(page_order=C.addressof(bad_order))), C.byref(h)) == 1
+    assert lib.oomb_pool_create(C.byref(_desc(offload=1)), C.byref(h)) == 1  # no staging buffers
+
+
+def test_allocator_host_logic(lib):
+    order = (C.c_int32 * 4)(2, 0, 3, 1)
+    h = C.c_void_p()
+    assert lib.oomb_pool_create(C.byref(_desc(page_order=C.addressof(order))), C.byref(h)) == 0
+    pool = h.value
+    assert lib.oomb_pool_free_pages(pool) == 4 and lib.oomb_pool_tokens(pool) == 0
+    fake = 1 << 24
+    # misaligned start, non-contiguous start, too many pages: refused before any device work
+    assert lib.oomb_kv_append(pool, fake, fake, 64, 128, None) == 1
+    assert lib.oomb_kv_append(pool, fake, fake, 0, 5 * 128, None) == 2
+    assert lib.oomb_kv_append(pool, fake + 8, fake, 0, 128, None) == 3
+    assert lib.oomb_pool_free_pages(pool) == 4
+    # chunk-level calls before the chunk's K/V exist
+    assert lib.oomb_chunk_attn_fwd(pool, fake, 0, 128, fake, fake, 8, 0.1, fake, fake, None) == 1
+    assert lib.oomb_page_select(pool, fake, 0, 128, 4, 1, fake, fake, 8, fake, 1 << 30, None) == 1
+    assert lib.oomb_prefetch(pool, fake, fake, 8, 0, None) == 8  # not an offload pool
+    assert lib.oomb_pool_set_stage(pool, 0) == 8
+    assert lib.oomb_workspace_size(pool, 0, 4096) > 0
+    assert lib.oomb_workspace_size(pool, 1, 4096) >= 28 * 4096 * 4
+    assert lib.oomb_workspace_size(pool, 9, 4096) == 0
+    tab = (C.c_int32 * 8)()
+    assert lib.oomb_page_table_host(pool, tab, 8) == 8 and list(tab) == [-1] * 8
+    lib.oomb_pool_destroy(pool)

@@ -1,0 +1,183 @@
+"""GPU parity: every step of the hot path through the C ABI against the fp64 oracle.
+
+Sizes span several pages and query tiles, with a ragged last chunk (partial last
+page).  Tolerances: relative L2 <= 1e-5 in fp32, <= 1e-2 in bf16 (O, LSE, dQ, dK,
+dV); page selection exact up to documented near-ties (relative score gap < 1e-4);
+pool copies bit-exact.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.oomb_oracle as O
+import paged_sparse_attention_gb300 as L
+from paged_sparse_attention_gb300 import synth
+from paged_sparse_attention_gb300.pool import PagedKVPool
+
+from harness import TOL, GpuSweep, f64, make_chunks, oracle_sweep
+
+pytestmark = pytest.mark.gpu
+
+QWEN = synth.WORKLOADS["sparse128k"]
+CASES = {
+    # fp32, tiny geometry (d 64, page 64, 2/1 heads), dense, ragged last chunk
+    "fp32_dense": synth.scaled(synth.WORKLOADS["tiny"], "fp32_dense", seq=1000, chunk=256),
+    # fp32 sparse, GQA 4:2, odd page size, partial page inside the last chunk
+    "fp32_sparse": synth.scaled(synth.WORKLOADS["tiny"], "fp32_sparse", n_q_heads=4, n_kv_heads=2, head_dim=32,
+                                seq=1111, chunk=240, page=48, top_k=3, plants=2),
+    # Qwen geometry bf16, dense, 4 chunks of 512 + ragged 200
+    "bf16_dense": synth.scaled(QWEN, "bf16_dense", seq=2248, chunk=512, top_k=-1, plants=0),
+    # Qwen geometry bf16, sparse top-4 with planted pages
+    "bf16_sparse": synth.scaled(QWEN, "bf16_sparse", seq=3000, chunk=512, top_k=4, plants=2),
+    # bf16 on a shape the tensor-core kernels do not take (d 64, page 64)
+    "bf16_small_d": synth.scaled(QWEN, "bf16_small_d", n_q_heads=6, n_kv_heads=2, head_dim=64, page=64,
+                                 seq=1300, chunk=320, top_k=3, plants=2),
+}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from paged_sparse_attention_gb300 import build
+    build.build()
+    L.load()
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_sweep_parity(name):
+    w = CASES[name]
+    chunks, plants = make_chunks(w)
+    order = synth.page_order(w).tolist()
+    ref = oracle_sweep(w, chunks, order)
+    run = GpuSweep(w, chunks, order, sel_override=ref["sel"])
+    assert run.err_bits == 0
+    tol = TOL[w.dtype]
+    for c in range(w.n_chunks):
+        assert O.rel_l2(f64(run.O[c]), ref["O"][c]) < tol, ("O", c)
+        assert O.rel_l2(f64(run.LSE[c]), ref["LSE"][c]) < tol, ("LSE", c)
+        assert O.rel_l2(f64(run.dQ[c]), ref["dQ"][c]) < tol, ("dQ", c)
+        # the reverse sweep's recomputed forward is bit-identical to the forward sweep
+        assert torch.equal(run.O[c], run.O2[c]) and torch.equal(run.LSE[c], run.LSE2[c])
+    rdk, rdv = ref["pool"].logical_grads()
+    assert O.rel_l2(f64(run.dK), rdk) < tol
+    assert O.rel_l2(f64(run.dV), rdv) < tol
+    # selection (GPU's own) against the oracle, up to near-ties
+    final = ref["pool"]
+    swaps = 0
+    for c in range(w.n_chunks):
+        start, n = w.chunk_bounds(c)
+        cand, scores = O.page_scores(final, chunks[c]["q"].double().numpy(), start, w.n_sink)
+        for h in range(w.n_kv_heads):
+            ok, k = O.near_tie_ok(run.gpu_sel[c][h], ref["sel"][c][h], cand, scores[h], w.top_k)
+            assert ok, (c, h, run.gpu_sel[c][h], ref["sel"][c][h])
+            swaps += k
+        if plants is not None:
+            for h in range(w.n_kv_heads):
+                for p in plants.planted.get((c, h), []):
+                    assert p in set(run.gpu_sel[c][h].tolist())
+    run.pool.close()
+
+
+@pytest.mark.parametrize("name", ["fp32_dense", "bf16_sparse"])
+def test_append_pools_bit_exact(name):
+    w = CASES[name]
+    chunks, _ = make_chunks(w)
+    order = synth.page_order(w)
+    dev = torch.device("cuda")
+    pool = PagedKVPool(w.n_q_heads, w.n_kv_heads, w.head_dim, w.page, w.num_phys, w.n_pages, w.torch_dtype,
+                       dev, page_order=order)
+    pool.dk_pool.fill_(7.0)
+    pool.dv_pool.fill_(7.0)
+    for c, ch in enumerate(chunks):
+        start, _ = w.chunk_bounds(c)
+        L.oomb_kv_append(pool.handle, ch["k"].to(dev), ch["v"].to(dev), start)
+    assert L.oomb_check(pool.handle) == 0
+    # page table = creation order, host copy == device table
+    tab = pool.table_host(w.n_pages)
+    assert tab == order[: w.n_pages].tolist()
+    assert pool.page_table[: w.n_pages].cpu().tolist() == tab
+    assert (pool.page_table[w.n_pages:].cpu() == -1).all()
+    k, v = pool.logical_kv(w.seq)
+    K = torch.cat([ch["k"] for ch in chunks])
+    V = torch.cat([ch["v"] for ch in chunks])
+    assert torch.equal(k.cpu(), K) and torch.equal(v.cpu(), V)
+    dk, dv = pool.logical_grads(w.seq)
+    assert (dk == 0).all() and (dv == 0).all()
+    # summaries: mean key over the tokens present (partial last page included)
+    Kd = K.double().numpy()
+    for p in range(w.n_pages):
+        m = min(w.page, w.seq - p * w.page)
+        ref = Kd[p * w.page: p * w.page + m].mean(axis=0)  # [Hkv, d]
+        got = f64(pool.summary[tab[p]])
+        np.testing.assert_allclose(got, ref, rtol=1e-5, atol=1e-6)
+    assert L.oomb_pool_free_pages(pool.handle) == w.num_phys - w.n_pages
+    pool.close()
+
+
+def test_select_edge_cases():
+    """top_k 0, top_k >= candidates, no sink, several sinks, first chunk."""
+    w = synth.scaled(QWEN, "edge", seq=128 * 12, chunk=128 * 3, top_k=2, plants=0)
+    chunks, _ = make_chunks(w)
+    order = synth.page_order(w)
+    dev = torch.device("cuda")
+    pool = PagedKVPool(w.n_q_heads, w.n_kv_heads, w.head_dim, w.page, w.num_phys, w.n_pages, w.torch_dtype,
+                       dev, page_order=order)
+    opool = O.OraclePool(w.n_kv_heads, w.head_dim, w.page, w.num_phys, w.n_pages)
+    ws = pool.workspace(L.OOMB_OP_SELECT, w.chunk)
+    used = 0
+    for c, ch in enumerate(chunks):
+        start, n = w.chunk_bounds(c)
+        L.oomb_kv_append(pool.handle, ch["k"].to(dev), ch["v"].to(dev), start)
+        npg = -(-n // w.page)
+        opool.append(ch["k"].double().numpy(), ch["v"].double().numpy(), start, order[used:used + npg].tolist())
+        used += npg
+        q = ch["q"].to(dev)
+        for top_k, n_sink in [(0, 1), (2, 0), (2, 3), (100, 1), (-1, 1), (1, 1)]:
+            max_sel = w.n_pages + 4
+            sel = torch.full((w.n_kv_heads, max_sel), -1, dtype=torch.int32, device=dev)
+            cnt = torch.zeros(w.n_kv_heads, dtype=torch.int32, device=dev)
+            L.oomb_page_select(pool.handle, q, start, top_k, n_sink, sel, cnt, ws)
+            ref = O.select_pages(opool, ch["q"].double().numpy(), start, top_k, n_sink)
+            cand, scores = O.page_scores(opool, ch["q"].double().numpy(), start, n_sink)
+            for h in range(w.n_kv_heads):
+                got = sel[h, : int(cnt[h])].cpu().numpy()
+                assert np.all(np.diff(got) > 0), "ascending"
+                ok, _ = O.near_tie_ok(got, ref[h], cand, scores[h], top_k)
+                assert ok, (c, top_k, n_sink, h, got, ref[h])
+    assert L.oomb_check(pool.handle) == 0
+    pool.close()
+
+
+def test_host_errors_on_gpu():
+    w = synth.scaled(QWEN, "err", seq=512, chunk=256, top_k=1, plants=0)
+    dev = torch.device("cuda")
+    pool = PagedKVPool(w.n_q_heads, w.n_kv_heads, w.head_dim, w.page, 3, 8, w.torch_dtype, dev)
+    ch = synth.make_chunk(w, 0)
+    k, v = ch["k"].to(dev), ch["v"].to(dev)
+    with pytest.raises(L.OombError) as e:
+        L.oomb_kv_append(pool.handle, k, v, 128)  # not contiguous with what is stored
+    assert e.value.status == 1
+    L.oomb_kv_append(pool.handle, k, v, 0)
+    with pytest.raises(L.OombError) as e:  # 2 more pages needed, 1 free
+        L.oomb_kv_append(pool.handle, k, v, 256)
+    assert e.value.status == 2
+    assert pool.n_tokens == 256
+    sel = torch.zeros((w.n_kv_heads, 1), dtype=torch.int32, device=dev)
+    cnt = torch.zeros(w.n_kv_heads, dtype=torch.int32, device=dev)
+    ws = pool.workspace(L.OOMB_OP_SELECT, 256)
+    with pytest.raises(L.OombError):  # max_sel 1 < 2 own pages
+        L.oomb_page_select(pool.handle, ch["q"].to(dev), 0, 1, 1, sel, cnt, ws)
+    # a selection index beyond the chunk raises the device error word, not a fault
+    bad = torch.tensor([[0, 5]] * w.n_kv_heads, dtype=torch.int32, device=dev)
+    bcnt = torch.full((w.n_kv_heads,), 2, dtype=torch.int32, device=dev)
+    o = torch.empty_like(ch["q"].to(dev))
+    lse = torch.empty(w.n_q_heads, 256, dtype=torch.float32, device=dev)
+    L.oomb_chunk_attn_fwd(pool.handle, ch["q"].to(dev), 0, bad, bcnt, 0.1, o, lse)
+    with pytest.raises(L.OombError) as e:
+        L.oomb_check(pool.handle)
+    assert e.value.status == 5
+    assert L.oomb_check(pool.handle) == 0  # cleared
+    pool.close()
