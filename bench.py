@@ -1,0 +1,396 @@
+"""Benchmark: one chunk-recurrent attention step (forward sweep + reverse sweep)
+of one attention layer through the liboomb C ABI on one GB300 per rank.
+
+A step = for every chunk in order: append K/V to the paged pool, select pages,
+forward attention; then for every chunk in reverse: recompute the forward and run
+the backward (dQ written, dK/dV accumulated into the paged fp32 gradient pool).
+This is the attention part of OOMB's chunk-recurrent training step ("Out of the
+Memory Barrier", gist.science explainer 2.A-2.D) for one layer.
+
+Metric: credited fwd+bwd attention TFLOP/s (14 d FLOPs per selected, causally
+visible (query, key) pair per query head; the recomputed forward is not credited)
+and tokens/s per layer.  Multi-GPU runs are independent replicas (the path has no
+exchange step); `value` sums all ranks.
+
+  python bench.py [--workload dense32k] [--steps K] [--warmup W] [--impl oomb|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged sparse chunk-attn fwd+bwd TFLOP/s and tokens/s/layer at 1 GB300; % roofline"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6783.0, "bf16_tflops": 1875.1, "bf16_tflops_sustained": 1690.3,
+                  "source": "driver-measured GB300 figures quoted in the repository's baseline notes"}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        d.setdefault("source", "MEASURED_PEAKS.json")
+        return d
+    return dict(FALLBACK_PEAKS)
+
+
+class ClockSampler:
+    """nvidia-smi SM clocks and throttle reasons, sampled every 200 ms."""
+
+    def __init__(self, index: int):
+        self.index, self.rows, self.proc = index, [], None
+
+    def __enter__(self):
+        q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 7:
+                self.rows.append(parts)
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[3 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+# ------------------------------------------------------------------ workload
+class Step:
+    """Device buffers and the per-chunk call sequence of one benchmark step."""
+
+    def __init__(self, w, dev, seed_offset=0):
+        import torch
+
+        import paged_sparse_attention_gb300 as L
+        from paged_sparse_attention_gb300 import synth
+        from paged_sparse_attention_gb300.pool import PagedKVPool
+
+        self.L, self.torch, self.w, self.dev = L, torch, w, dev
+        self.scale = 1.0 / math.sqrt(w.head_dim)
+        order = synth.page_order(w)
+        self.pool = PagedKVPool(w.n_q_heads, w.n_kv_heads, w.head_dim, w.page, w.num_phys, w.n_pages,
+                                w.torch_dtype, dev, page_order=order)
+        plants = synth.PlantTable(w) if w.plants > 0 else None
+        # inputs generated on the device, per chunk (seeded), resident for the whole run
+        self.chunks = []
+        for c in range(w.n_chunks):
+            self.chunks.append(synth.make_chunk(w, c, device=dev, plants=plants))
+        C = w.chunk
+        self.ws_sel = self.pool.workspace(L.OOMB_OP_SELECT, C)
+        self.ws_bwd = self.pool.workspace(L.OOMB_OP_BWD, C)
+        self.sel = torch.full((w.n_chunks, w.n_kv_heads, w.max_sel), -1, dtype=torch.int32, device=dev)
+        self.cnt = torch.zeros((w.n_chunks, w.n_kv_heads), dtype=torch.int32, device=dev)
+        self.o = torch.empty((C, w.n_q_heads, w.head_dim), dtype=w.torch_dtype, device=dev)
+        self.lse = torch.empty((w.n_q_heads, C), dtype=torch.float32, device=dev)
+        self.dq = [torch.empty_like(ch["q"]) for ch in self.chunks]
+        self.fwd_events, self.bwd_events = [], []
+
+    def run(self, record=False):
+        L, w, h = self.L, self.w, self.pool.handle
+        torch = self.torch
+        L.oomb_pool_reset(h)
+        for c, ch in enumerate(self.chunks):
+            start, n = w.chunk_bounds(c)
+            L.oomb_kv_append(h, ch["k"], ch["v"], start)
+            L.oomb_page_select(h, ch["q"], start, w.top_k, w.n_sink, self.sel[c], self.cnt[c], self.ws_sel)
+            self._fwd(c, ch, start, n, record)
+        for c in range(w.n_chunks - 1, -1, -1):
+            ch = self.chunks[c]
+            start, n = w.chunk_bounds(c)
+            self._fwd(c, ch, start, n, record)  # recompute (activations are not kept)
+            if record:
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+            lse = self.lse if n == w.chunk else self.lse_tail(n)
+            L.oomb_chunk_attn_bwd(h, ch["q"], self.o[:n], ch["do"], lse, start, self.sel[c], self.cnt[c],
+                                  self.scale, self.dq[c], self.ws_bwd)
+            if record:
+                e1.record()
+                self.bwd_events.append((e0, e1, c))
+
+    def _fwd(self, c, ch, start, n, record):
+        L, torch = self.L, self.torch
+        if record:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+        lse = self.lse if n == self.w.chunk else self.lse_tail(n)
+        L.oomb_chunk_attn_fwd(self.pool.handle, ch["q"], start, self.sel[c], self.cnt[c], self.scale,
+                              self.o[:n], lse)
+        if record:
+            e1.record()
+            self.fwd_events.append((e0, e1, c))
+
+    def lse_tail(self, n):
+        if not hasattr(self, "_lse_tail") or self._lse_tail.shape[1] != n:
+            self._lse_tail = self.torch.empty((self.w.n_q_heads, n), dtype=self.torch.float32, device=self.dev)
+        return self._lse_tail
+
+    def pairs_per_chunk(self):
+        """Selected, causally visible (query, key) pairs summed over query heads, per chunk."""
+        w = self.w
+        sel, cnt = self.sel.cpu(), self.cnt.cpu()
+        out = []
+        for c in range(w.n_chunks):
+            start, n = w.chunk_bounds(c)
+            first_own = start // w.page
+            tot = 0
+            for hk in range(w.n_kv_heads):
+                for p in sel[c, hk, : int(cnt[c, hk])].tolist():
+                    k0 = p * w.page
+                    k1 = min(k0 + w.page, start + n)
+                    if p < first_own:
+                        tot += (k1 - k0) * n
+                    else:  # own page: row i (absolute start+i) sees keys <= start+i
+                        for kpos in range(k0, k1):
+                            tot += start + n - kpos
+            out.append(tot * w.group)
+        return out
+
+
+def oracle_sample_seconds(w, budget_s=20.0):
+    """Time the fp64 CPU oracle on a bounded sample: the forward+backward of chunk 1
+    (or 0) for the query heads of KV group 0, repeated until ``budget_s``."""
+    import numpy as np
+    import torch
+
+    import oracle.oomb_oracle as O
+    from paged_sparse_attention_gb300 import synth
+
+    c = 1 if w.n_chunks > 1 else 0
+    plants = synth.PlantTable(w) if w.plants > 0 else None
+    chunks = [synth.make_chunk(w, i, plants=plants) for i in range(c + 1)]
+    G = w.group
+    pool = O.OraclePool(1, w.head_dim, w.page, w.num_phys, w.n_pages)
+    order = synth.page_order(w).tolist()
+    used = 0
+    for i, ch in enumerate(chunks):
+        start, n = w.chunk_bounds(i)
+        npg = -(-n // w.page)
+        pool.append(ch["k"][:, :1].double().numpy(), ch["v"][:, :1].double().numpy(), start, order[used:used + npg])
+        used += npg
+    start, n = w.chunk_bounds(c)
+    q = chunks[c]["q"][:, :G].double().numpy()
+    do = chunks[c]["do"][:, :G].double().numpy()
+    sel = O.select_pages(pool, q, start, w.top_k, w.n_sink)
+    scale = 1.0 / math.sqrt(w.head_dim)
+    # credited pairs of the sample
+    kpos = np.concatenate([p * w.page + np.arange(pool.tokens_in_page(p)) for p in sel[0]])
+    pairs = int(sum(int((kpos <= start + i).sum()) for i in range(n))) * G
+    flops = pairs * 14 * w.head_dim
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        o, lse = O.chunk_attn_fwd(pool, q, start, sel, scale)
+        O.chunk_attn_bwd(pool, q, o, do, lse, start, sel, scale)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el > budget_s or reps >= 50:
+            break
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    sample = (f"chunk {c} ({n} queries) fwd+bwd for the {G} query heads of KV group 0, "
+              f"{reps} repetition(s), fp64 numpy")
+    return {"seconds": el / reps, "flops": flops, "cores": cores, "sample": sample, "tokens": n / w.n_kv_heads}
+
+
+def run_reference(args, w, rank, world):
+    """The CPU oracle as it stands, on host cores, on a bounded sample per step."""
+    if rank != 0:
+        return
+    res = []
+    for _ in range(args.warmup if args.warmup < 1 else 1):
+        oracle_sample_seconds(w, budget_s=1.0)
+    for _ in range(args.steps):
+        res.append(oracle_sample_seconds(w, budget_s=max(2.0, 20.0 / max(1, args.steps))))
+    sec = statistics.mean(r["seconds"] for r in res)
+    tflops = res[0]["flops"] / sec / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": tflops, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "seq": w.seq, "chunk": w.chunk, "page": w.page, "top_k": w.top_k,
+                       "heads": f"{w.n_q_heads}/{w.n_kv_heads}", "head_dim": w.head_dim},
+            "cpu_baseline": {"value": tflops, "unit": UNIT, "cores": res[0]["cores"], "kind": "oracle",
+                             "sample": res[0]["sample"]},
+            "e2e": {"value": tflops, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="oomb", choices=["oomb", "reference"])
+    ap.add_argument("--workload", default="dense32k")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    from paged_sparse_attention_gb300 import synth
+    w = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w, rank, world)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import paged_sparse_attention_gb300 as L
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    step = Step(w, dev)
+    for _ in range(max(3, args.warmup)):
+        step.run()
+    torch.cuda.synchronize()
+    L.oomb_check(step.pool.handle)
+    pairs = step.pairs_per_chunk()
+    credited = sum(pairs) * 14 * w.head_dim
+    fwd_flops = {c: p * 4 * w.head_dim for c, p in enumerate(pairs)}
+    bwd_flops = {c: p * 10 * w.head_dim for c, p in enumerate(pairs)}
+
+    # ---- timed region (device-resident inputs; the step's inputs exceed L2) ----
+    launches0 = L.oomb_launch_count()
+    with ClockSampler(local) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            step.run(record=True)
+        e1.record()
+        torch.cuda.synchronize()
+        barrier()
+    launches = L.oomb_launch_count() - launches0
+    ms = e0.elapsed_time(e1) / args.steps
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms = float(t.item())
+    L.oomb_check(step.pool.handle)
+
+    # per-kernel-call roofline: the backward (dominant) and forward calls
+    bwd_ms = [a.elapsed_time(b) for a, b, _ in step.bwd_events]
+    bwd_fl = [bwd_flops[c] for _, _, c in step.bwd_events]
+    fwd_ms = [a.elapsed_time(b) for a, b, _ in step.fwd_events]
+    fwd_fl = [fwd_flops[c] for _, _, c in step.fwd_events]
+    peaks = load_peaks()
+    bwd_tflops = sum(bwd_fl) / (sum(bwd_ms) * 1e-3) / 1e12
+    fwd_tflops = sum(fwd_fl) / (sum(fwd_ms) * 1e-3) / 1e12
+    peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+    value = credited / (ms * 1e-3) / 1e12 * world
+    tokens_per_s = w.seq / (ms * 1e-3) * world
+
+    line = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": round(ms, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "fp32",
+            "data": "synthetic (seeded N(0,1) Q/K/V/dO, RoPE theta 1e6; no trained weights)",
+            "config": {"workload": w.name, "seq": w.seq, "chunk": w.chunk, "page": w.page, "top_k": w.top_k,
+                       "heads": f"{w.n_q_heads}/{w.n_kv_heads}", "head_dim": w.head_dim,
+                       "parallelism": "replicas" if world > 1 else "single",
+                       "l2": "inputs larger than L2 (Q+dO alone exceed 129 MB)",
+                       "attention_kernels": "tcgen05" if L.oomb_uses_tensor_cores(step.pool.handle) else "simt"},
+            "tokens_per_s_per_layer": round(tokens_per_s, 1),
+            "credited_tflop_per_step": credited / 1e12,
+            "fwd_call_tflops": round(fwd_tflops, 2), "bwd_call_tflops": round(bwd_tflops, 2),
+            "roofline": {"bound": "tensor", "kernel": "oomb_chunk_attn_bwd", "achieved": round(bwd_tflops, 2),
+                         "peak": peak, "unit": "TFLOP/s", "frac": round(bwd_tflops / peak, 4),
+                         "peak_source": peaks.get("source", "") + " (bf16 dense, sustained)",
+                         "traffic": None},
+            "gpu_launches": int(launches),
+            "clocks": clk.summary()}
+
+    if not args.no_e2e:
+        line["e2e"] = measure_e2e(step, args.steps, credited, world, dev)
+    if rank == 0 and not args.no_cpu_baseline and world == 1:
+        cb = oracle_sample_seconds(w, budget_s=15.0)
+        line["cpu_baseline"] = {"value": cb["flops"] / cb["seconds"] / 1e12, "unit": UNIT, "cores": cb["cores"],
+                                "kind": "oracle", "sample": cb["sample"]}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def measure_e2e(step, steps, credited, world, dev):
+    """Same step with host-resident inputs: every step copies Q, K, V, dO of all
+    chunks from pinned host memory to the device and reads dQ and the dK/dV pools
+    back, all inside the timed region."""
+    import torch
+    host_in = [{k: v.cpu().pin_memory() for k, v in ch.items()} for ch in step.chunks]
+    host_dq = [torch.empty(d.shape, dtype=d.dtype).pin_memory() for d in step.dq]
+    host_dk = torch.empty(step.pool.dk_pool.shape, dtype=torch.float32).pin_memory()
+    host_dv = torch.empty(step.pool.dv_pool.shape, dtype=torch.float32).pin_memory()
+    bi = sum(t.numel() * t.element_size() for ch in host_in for t in ch.values())
+    bo = sum(t.numel() * t.element_size() for t in host_dq) + 2 * host_dk.numel() * 4
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        for ch, hc in zip(step.chunks, host_in):
+            for k in ch:
+                ch[k].copy_(hc[k], non_blocking=True)
+        step.run()
+        for d, hd in zip(step.dq, host_dq):
+            hd.copy_(d, non_blocking=True)
+        host_dk.copy_(step.pool.dk_pool, non_blocking=True)
+        host_dv.copy_(step.pool.dv_pool, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return {"value": round(credited / (ms * 1e-3) / 1e12 * world, 3), "unit": UNIT, "ms_per_step": round(ms, 3),
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
+
+
+if __name__ == "__main__":
+    main()

@@ -200,6 +200,9 @@ OOMB_API int oomb_pool_free_pages(const oomb_pool* pool);
 
 OOMB_API const char* oomb_status_str(oomb_status s);
 
+/* Kernels this library has launched since it was loaded (all pools, all devices). */
+OOMB_API uint64_t oomb_launch_count(void);
+
 /* Which attention kernels a call with this pool would use: 1 = tcgen05, 0 = SIMT. */
 OOMB_API int oomb_uses_tensor_cores(const oomb_pool* pool);
 

@@ -73,6 +73,7 @@ def load(path: str = LIB_PATH) -> C.CDLL:
         "oomb_pool_free_pages": (i32, [vp]),
         "oomb_status_str": (C.c_char_p, [i32]),
         "oomb_uses_tensor_cores": (i32, [vp]),
+        "oomb_launch_count": (C.c_uint64, []),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -183,3 +184,7 @@ def oomb_pool_free_pages(pool: int) -> int:
 
 def oomb_uses_tensor_cores(pool: int) -> bool:
     return bool(load().oomb_uses_tensor_cores(pool))
+
+
+def oomb_launch_count() -> int:
+    return int(load().oomb_launch_count())

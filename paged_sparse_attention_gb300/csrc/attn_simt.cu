@@ -358,6 +358,7 @@ template <typename T>
 cudaError_t fwd_simt(const AttnArgs& a, cudaStream_t st) {
   dim3 grid((a.n_q + kRowsPerBlock - 1) / kRowsPerBlock, a.g.Hq);
   fwd_rows<T><<<grid, kRowsPerBlock * 32, 0, st>>>(a);
+  count_launches(1);
   return cudaGetLastError();
 }
 
@@ -373,6 +374,7 @@ cudaError_t bwd_simt(const AttnArgs& a, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(bwd_dkdv<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)shb);
   if (e != cudaSuccess) return e;
   bwd_dkdv<T><<<gk, kDkdvThreads, shb, st>>>(a, Dbuf);
+  count_launches(3);
   return cudaGetLastError();
 }
 

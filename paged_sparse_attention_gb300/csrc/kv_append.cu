@@ -121,6 +121,7 @@ cudaError_t launch_kv_append(const Geometry& g, void* k_pool, void* v_pool, floa
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    count_launches(1);
   }
   return cudaSuccess;
 }

@@ -1,5 +1,6 @@
 // C-ABI layer: pool object, host-side page allocator, argument checks and
 // dispatch to the kernels.  No call here allocates device memory.
+#include <atomic>
 #include <cstring>
 #include <new>
 
@@ -17,6 +18,12 @@ struct oomb_pool {
   int stage_buf = 0;
   bool table_dirty = true;  // device page table still needs its -1 fill
 };
+
+namespace {
+std::atomic<uint64_t> g_launches{0};
+}  // namespace
+
+void oomb::count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 
 namespace {
 
@@ -164,6 +171,8 @@ int oomb_page_table_host(const oomb_pool* p, int32_t* out, int n) {
   std::memcpy(out, p->table.data(), sizeof(int32_t) * (size_t)m);
   return m;
 }
+
+uint64_t oomb_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 int oomb_uses_tensor_cores(const oomb_pool* p) { return p && tc_supported(p->g) ? 1 : 0; }
 

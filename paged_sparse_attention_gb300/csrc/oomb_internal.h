@@ -74,6 +74,9 @@ cudaError_t launch_prefetch(const Geometry& g, const void* k_pool, const void* v
                             int stage_h0, int stage_stride, uint32_t* err, cudaStream_t st);
 
 __host__ __device__ inline size_t dtype_size(int dt) { return dt == OOMB_FP32 ? 4 : 2; }
+// Count of kernel launches issued by the library (reported by oomb_launch_count).
+void count_launches(int n);
+
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 }  // namespace oomb

@@ -288,9 +288,11 @@ cudaError_t launch_page_select(const Geometry& g, const float* summary, const in
     qbar_reduce<<<(int)((HD + 255) / 256), 256, 0, st>>>(g, partial, nb, 1.0f / ((float)n_q * g.G), qbar);
     dim3 sg((n_cand + kScoreWarps - 1) / kScoreWarps, g.Hkv);
     page_score<<<sg, kScoreWarps * 32, 0, st>>>(g, qbar, summary, table, cand0, n_cand, score_stride, scores, err);
+    count_launches(3);
   }
   topk_select<<<g.Hkv, kTopkThreads, 0, st>>>(g, scores, score_stride, n_sinks, cand0, n_cand, top_k, own0, n_own,
                                                sel, sel_count, max_sel);
+  count_launches(1);
   return cudaGetLastError();
 }
 

@@ -60,6 +60,7 @@ cudaError_t launch_prefetch(const Geometry& g, const void* k_pool, const void* v
   gather_pages<<<grid, kPrefetchThreads, 0, st>>>(g, (const uint8_t*)k_pool, (const uint8_t*)v_pool, table, sel,
                                                   sel_count, max_sel, (uint8_t*)stage_k, (uint8_t*)stage_v,
                                                   stage_h0, stage_stride, err);
+  count_launches(1);
   return cudaGetLastError();
 }
 

