@@ -1,8 +1,468 @@
-// tcgen05 chunk-attention backward (bf16, head_dim 128, page 128).
+// tcgen05 chunk-attention backward (bf16 in, fp32 accumulate; head_dim 128, page 128).
+//
+// "Out of the Memory Barrier" (gist.science explainer): the backward recomputes the
+// attention probabilities on the fly (2.A) and accumulates the key/value gradients
+// in place in the paged gradient pool that shares the KV page table (2.B).
+//
+// Kernels of one backward call:
+//   bwd_prep     D_i = dO_i . O_i (fp32) and zero the fp32 dQ accumulator
+//   bwd_main     one CTA per (selected page, KV head): K and V of the page stay in
+//                shared memory; the CTA walks every 128-row query tile that can see
+//                the page, for each of the G query heads of the group, in two
+//                64-row halves:
+//                  S^T  = K Q_h^T       dP^T = V dO_h^T          (TMEM, fp32)
+//                  P^T  = exp2(S^T scale log2e - LSE log2e)     (masked on the diagonal)
+//                  dS^T = P^T (dP^T - D)
+//                  dV  += P^T dO_h      dK  += dS^T Q_h          (A operands from TMEM)
+//                  dQ^T = K^T dS^T      (dS^T also written to shared memory as the B
+//                                        operand; dQ^T read out, staged and bulk-added
+//                                        to the fp32 accumulator in global memory)
+//                and finally adds scale*dK and dV into the block's own rows of the
+//                fp32 gradient pool: no two CTAs own the same rows, so dK/dV need no
+//                atomics.
+//   bwd_convert  dq = bf16(scale * dQ accumulator), token-major.
+//
+// Warp roles of bwd_main (320 threads):
+//   warp 0     TMA producer (K, V once; then a ring of Q/dO half tiles + LSE/D)
+//   warp 1     TMEM owner and MMA issuer
+//   warps 2-5  softmax: thread == key row (TMEM lane); epilogue for dK/dV
+//   warps 6-9  dQ read-out: thread == head-dim column (TMEM lane of dQ^T)
+// TMEM columns: half a [0,128), half b [128,256): S^T [0,64) dP^T [64,128), then
+// P^T [0,32) dS^T [32,64) dQ^T [64,128); dV [256,384); dK [384,512).
 #include "tc_common.cuh"
 
 namespace oomb {
+namespace {
 
-cudaError_t launch_attn_bwd_tc(const AttnArgs& a, cudaStream_t st) { return launch_attn_bwd_simt(a, st); }
+using namespace tc;
+
+constexpr int kRing = 3;
+constexpr int kHalf = 64;
+constexpr uint32_t kHalfTile = kHalf * kD * 2;  // 16 KB: one 64-row half tile (two 8 KB boxes)
+constexpr uint32_t kHalfBox = kHalfTile / 2;
+constexpr int kThreads = 320;
+constexpr int kPieceRows = 16;                   // dQ rows per bulk reduce
+constexpr uint32_t kPieceBytes = kPieceRows * kD * 4;
+
+struct BwdParams {
+  const int32_t* sel;
+  const int32_t* sel_count;
+  const int32_t* table;
+  const float* lse;
+  const float* Dbuf;
+  float* dq_acc;
+  float* dk_pool;
+  float* dv_pool;
+  uint32_t* err;
+  int max_sel, n_q, Hq, G, Hkv, num_phys, max_logical, n_tiles;
+  int64_t q_start;
+  float scale, scale_log2;
+  int staged, stage_h0, stage_stride;
+};
+
+struct __align__(8) BwdBarriers {
+  uint64_t kv_full;
+  uint64_t hs_full[kRing];
+  uint64_t hs_empty[kRing];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t dq_full[2];
+  uint64_t dq_free[2];
+  uint64_t acc_full;
+  uint32_t tmem_base;
+  int abort;
+};
+
+// shared memory map (offsets from the 1024-aligned base)
+constexpr uint32_t kOffK = 0;
+constexpr uint32_t kOffV = kOffK + kTileBytes;
+constexpr uint32_t kOffRing = kOffV + kTileBytes;                 // kRing x (Q half, dO half)
+constexpr uint32_t kOffDS = kOffRing + kRing * 2 * kHalfTile;     // 2 x dS^T half [128 keys][64 q]
+constexpr uint32_t kOffStage = kOffDS + 2 * kHalfTile;            // 2 x dQ pieces
+constexpr uint32_t kOffVec = kOffStage + 2 * kPieceBytes;         // kRing x (lse2[64], D[64])
+constexpr uint32_t kOffBar = kOffVec + kRing * 2 * kHalf * 4;
+constexpr size_t kSmemBytes = 1024 + kOffBar + sizeof(BwdBarriers);
+
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
+                       const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
+                       const BwdParams p) {
+  const int s = blockIdx.x, h = blockIdx.y;
+  if (s >= p.sel_count[h]) return;
+  const int first_own = (int)(p.q_start / kTile);
+  const int nvis = (int)((p.q_start + p.n_q + kTile - 1) / kTile);
+  const int pg = p.sel[(size_t)h * p.max_sel + s];
+  if (pg < 0 || pg >= nvis || pg >= p.max_logical) {
+    if (threadIdx.x == 0) atomicOr(p.err, OOMB_DEVERR_SEL);
+    return;
+  }
+  const int phys = p.table[pg];
+  if (phys < 0 || phys >= p.num_phys) {
+    if (threadIdx.x == 0) atomicOr(p.err, OOMB_DEVERR_PAGE);
+    return;
+  }
+  const int own = pg - first_own;           // >= 0 for the chunk's own pages
+  const int t0 = own > 0 ? own : 0;
+  const int n_steps = (p.n_tiles - t0) * p.G;
+  if (n_steps <= 0) return;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  BwdBarriers* bar = reinterpret_cast<BwdBarriers*>(sm + kOffBar);
+  float* vec = reinterpret_cast<float*>(sm + kOffVec);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  volatile int* abort = &bar->abort;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bar->kv_full, 1);
+    for (int i = 0; i < kRing; ++i) {
+      mbar_init(&bar->hs_full[i], 1);
+      mbar_init(&bar->hs_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar->s_full[i], 1);
+      mbar_init(&bar->p_full[i], 128);
+      mbar_init(&bar->dq_full[i], 1);
+      mbar_init(&bar->dq_free[i], 128);
+    }
+    mbar_init(&bar->acc_full, 1);
+    bar->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bar->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bar->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tq);
+      tma_prefetch_desc(&tdo);
+      const int64_t blk = p.staged ? (int64_t)(p.stage_h0 + h) * p.stage_stride + s : (int64_t)phys * p.Hkv + h;
+      const int row = (int)(blk * kTile);
+      mbar_arrive_expect_tx(&bar->kv_full, 2 * kTileBytes);
+      tma_load_2d(sm + kOffK, &tk, &bar->kv_full, 0, row);
+      tma_load_2d(sm + kOffK + kHalfBytes, &tk, &bar->kv_full, 64, row);
+      tma_load_2d(sm + kOffV, &tv, &bar->kv_full, 0, row);
+      tma_load_2d(sm + kOffV + kHalfBytes, &tv, &bar->kv_full, 64, row);
+    }
+    bool ok = true;
+    int v = 0;
+    for (; v < 2 * n_steps; ++v) {
+      const int slot = v % kRing;
+      if (v >= kRing) {
+        if (lane == 0) ok = mbar_wait(&bar->hs_empty[slot], ((v / kRing) - 1) & 1, p.err, abort);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+      }
+      const int u = v >> 1, hh = v & 1;
+      const int t = t0 + u / p.G, g = u % p.G;
+      const int hq = h * p.G + g;
+      const int q0 = t * kTile + hh * kHalf;
+      float* vs = vec + slot * 2 * kHalf;
+      for (int i = lane; i < kHalf; i += 32) {
+        const int qi = q0 + i;
+        const bool valid = qi < p.n_q;
+        vs[i] = valid ? p.lse[(size_t)hq * p.n_q + qi] * kLog2e : INFINITY;
+        vs[kHalf + i] = valid ? p.Dbuf[(size_t)hq * p.n_q + qi] : 0.f;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        uint8_t* dst = sm + kOffRing + slot * 2 * kHalfTile;
+        mbar_arrive_expect_tx(&bar->hs_full[slot], 2 * kHalfTile);
+        tma_load_3d(dst, &tq, &bar->hs_full[slot], 0, hq, q0);
+        tma_load_3d(dst + kHalfBox, &tq, &bar->hs_full[slot], 64, hq, q0);
+        tma_load_3d(dst + kHalfTile, &tdo, &bar->hs_full[slot], 0, hq, q0);
+        tma_load_3d(dst + kHalfTile + kHalfBox, &tdo, &bar->hs_full[slot], 64, hq, q0);
+      }
+    }
+    if (lane == 0) {  // drain the copies still in flight before the CTA may exit
+      for (int vv = (v > kRing ? v - kRing : 0); vv < v; ++vv)
+        mbar_wait(&bar->hs_full[vv % kRing], (vv / kRing) & 1, p.err, nullptr);
+      mbar_wait(&bar->kv_full, 0, p.err, nullptr);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t id_s = idesc_bf16_f32(128, 64, false, false);   // S^T, dP^T
+      const uint32_t id_acc = idesc_bf16_f32(128, 128, false, true);  // dV, dK (A from TMEM)
+      const uint32_t id_dq = idesc_bf16_f32(128, 64, true, true);     // dQ^T
+      const uint32_t aK = smem_u32(sm + kOffK), aV = smem_u32(sm + kOffV);
+      bool ok = mbar_wait(&bar->kv_full, 0, p.err, abort);
+      bool first_acc = true;
+      for (int u = 0; ok && u < n_steps; ++u) {
+        for (int hh = 0; hh < 2 && ok; ++hh) {
+          const int v = 2 * u + hh, slot = v % kRing;
+          ok = mbar_wait(&bar->hs_full[slot], (v / kRing) & 1, p.err, abort);
+          if (ok && u > 0) ok = mbar_wait(&bar->dq_free[hh], (u - 1) & 1, p.err, abort);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t aQ = smem_u32(sm + kOffRing + slot * 2 * kHalfTile);
+          const uint32_t adO = aQ + kHalfTile;
+          const uint32_t tS = tmem + hh * 128;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tS, desc_kmajor(aK, kk), desc_kmajor(aQ, kk, kHalfBox), id_s, kk > 0);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tS + 64, desc_kmajor(aV, kk), desc_kmajor(adO, kk, kHalfBox), id_s, kk > 0);
+          mma_commit(&bar->s_full[hh]);
+        }
+        for (int hh = 0; hh < 2 && ok; ++hh) {
+          const int v = 2 * u + hh, slot = v % kRing;
+          ok = mbar_wait(&bar->p_full[hh], u & 1, p.err, abort);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t aQ = smem_u32(sm + kOffRing + slot * 2 * kHalfTile);
+          const uint32_t adO = aQ + kHalfTile;
+          const uint32_t tS = tmem + hh * 128;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            mma_ts(tmem + 256, tS + kk * 8, desc_mnmajor(adO, kk, kHalfBox), id_acc, first_acc ? 0u : 1u);
+            mma_ts(tmem + 384, tS + 32 + kk * 8, desc_mnmajor(aQ, kk, kHalfBox), id_acc, first_acc ? 0u : 1u);
+            first_acc = false;
+          }
+          mma_commit(&bar->hs_empty[slot]);
+          const uint32_t adS = smem_u32(sm + kOffDS + hh * kHalfTile);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tS + 64, desc_mnmajor(aK, kk), desc_mnmajor(adS, kk, kHalfBox), id_dq, kk > 0);
+          mma_commit(&bar->dq_full[hh]);
+        }
+      }
+      mma_commit(&bar->acc_full);
+      mbar_wait(&bar->acc_full, 0, p.err, nullptr);
+    }
+  } else if (warp < 6) {
+    // ------------------------------------------------------------------ softmax
+    const int j = (warp & 3) * 32 + lane;  // key row of the page
+    const uint32_t lane_off = tmem_lane_base(warp);
+    bool ok = true;
+    for (int u = 0; ok && u < n_steps; ++u) {
+      const int t = t0 + u / p.G;
+      const bool diag = (own >= 0) && (t == own);
+      for (int hh = 0; hh < 2; ++hh) {
+        const int v = 2 * u + hh, slot = v % kRing;
+        ok = mbar_wait(&bar->s_full[hh], u & 1, p.err, abort) &&
+             mbar_wait(&bar->hs_full[slot], (v / kRing) & 1, p.err, abort);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t sr[64], dr[64];
+        {
+          const uint32_t base = tmem + lane_off + hh * 128;
+          tmem_ld32(base + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+          tmem_ld32(base + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+          tmem_ld32(base + 64, *reinterpret_cast<uint32_t(*)[32]>(&dr[0]));
+          tmem_ld32(base + 96, *reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
+          tmem_wait_ld();
+        }
+        const float* vs = vec + slot * 2 * kHalf;
+        uint32_t pk[32], dk[32];
+        const int qbase = hh * kHalf;  // query row (within the tile) of column 0
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          float pr[2], dsr[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int i = 2 * c + e;
+            float pv = exp2f(fmaf(__uint_as_float(sr[i]), p.scale_log2, -vs[i]));
+            if (diag && j > qbase + i) pv = 0.f;
+            pr[e] = pv;
+            dsr[e] = pv * (__uint_as_float(dr[i]) - vs[kHalf + i]);
+          }
+          pk[c] = pack_bf16x2(pr[0], pr[1]);
+          dk[c] = pack_bf16x2(dsr[0], dsr[1]);
+        }
+        const uint32_t base = tmem + lane_off + hh * 128;
+        tmem_st32(base + 0, pk);
+        tmem_st32(base + 32, dk);
+        // dS^T row j (64 query columns) into the swizzled B-operand tile of the dQ^T MMA
+        uint8_t* drow = sm + kOffDS + hh * kHalfTile + j * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint4 w = make_uint4(dk[4 * c], dk[4 * c + 1], dk[4 * c + 2], dk[4 * c + 3]);
+          *reinterpret_cast<uint4*>(drow + ((c ^ (j & 7)) * 16)) = w;
+        }
+        tmem_wait_st();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&bar->p_full[hh]);
+      }
+    }
+    // epilogue: this CTA's rows of the gradient pool += scale * dK, dV
+    if (ok && mbar_wait(&bar->acc_full, 0, p.err, abort)) {
+      tc_fence_after();
+      const size_t row = (((size_t)phys * p.Hkv + h) * kTile + j) * kD;
+      float4* gdv = reinterpret_cast<float4*>(p.dv_pool + row);
+      float4* gdk = reinterpret_cast<float4*>(p.dk_pool + row);
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t a[32], b[32];
+        tmem_ld32(tmem + lane_off + 256 + cc * 32, a);
+        tmem_ld32(tmem + lane_off + 384 + cc * 32, b);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          float4 x = gdv[cc * 8 + e];
+          x.x += __uint_as_float(a[4 * e]);
+          x.y += __uint_as_float(a[4 * e + 1]);
+          x.z += __uint_as_float(a[4 * e + 2]);
+          x.w += __uint_as_float(a[4 * e + 3]);
+          gdv[cc * 8 + e] = x;
+          float4 y = gdk[cc * 8 + e];
+          y.x += p.scale * __uint_as_float(b[4 * e]);
+          y.y += p.scale * __uint_as_float(b[4 * e + 1]);
+          y.z += p.scale * __uint_as_float(b[4 * e + 2]);
+          y.w += p.scale * __uint_as_float(b[4 * e + 3]);
+          gdk[cc * 8 + e] = y;
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------------ dQ read-out
+    const int col = (warp & 3) * 32 + lane;  // head-dim column == TMEM lane of dQ^T
+    const uint32_t lane_off = tmem_lane_base(warp);
+    const bool leader = (warp == 6 && lane == 0);
+    float* stage = reinterpret_cast<float*>(sm + kOffStage);
+    bool ok = true;
+    int piece = 0;
+    for (int u = 0; ok && u < n_steps; ++u) {
+      const int t = t0 + u / p.G, g = u % p.G;
+      const int hq = h * p.G + g;
+      for (int hh = 0; hh < 2; ++hh) {
+        ok = mbar_wait(&bar->dq_full[hh], u & 1, p.err, abort);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t r[64];
+        tmem_ld32(tmem + lane_off + hh * 128 + 64, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+        tmem_ld32(tmem + lane_off + hh * 128 + 96, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&bar->dq_free[hh]);
+        const int q0 = t * kTile + hh * kHalf;
+#pragma unroll
+        for (int pc = 0; pc < kHalf / kPieceRows; ++pc, ++piece) {
+          const int buf = piece & 1;
+          if (leader) bulk_wait_read<1>();  // the reduce that last read this buffer is done
+          named_bar_sync(1, 128);
+          float* st = stage + buf * (kPieceRows * kD);
+#pragma unroll
+          for (int rr = 0; rr < kPieceRows; ++rr) st[rr * kD + col] = __uint_as_float(r[pc * kPieceRows + rr]);
+          fence_proxy_async_smem();
+          named_bar_sync(1, 128);
+          if (leader) {
+            const int r0 = q0 + pc * kPieceRows;
+            const int nrows = min(kPieceRows, p.n_q - r0);
+            if (nrows > 0) {
+              bulk_reduce_add_f32(p.dq_acc + ((size_t)hq * p.n_q + r0) * kD, st, (uint32_t)nrows * kD * 4);
+            }
+            bulk_commit();
+          }
+        }
+      }
+    }
+    if (leader) bulk_wait<0>();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// D = rowsum(dO * O) per (row, head); dq_acc rows zeroed.  One warp per (row, head).
+__global__ void bwd_prep(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout, int n_q,
+                         int Hq, float* __restrict__ Dbuf, float* __restrict__ dq_acc) {
+  const int w = (blockIdx.x * blockDim.x + threadIdx.x) / 32, lane = threadIdx.x % 32;
+  if (w >= n_q * Hq) return;
+  const int i = w / Hq, hq = w % Hq;
+  const size_t off = ((size_t)i * Hq + hq) * kD + lane * 4;
+  const uint2 a = *reinterpret_cast<const uint2*>(o + off);
+  const uint2 b = *reinterpret_cast<const uint2*>(dout + off);
+  const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+  const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+  float s = 0.f;
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    const float2 x = __bfloat1622float2(a2[e]), y = __bfloat1622float2(b2[e]);
+    s += x.x * y.x + x.y * y.y;
+  }
+#pragma unroll
+  for (int off2 = 16; off2 > 0; off2 >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off2);
+  if (lane == 0) Dbuf[(size_t)hq * n_q + i] = s;
+  reinterpret_cast<float4*>(dq_acc + ((size_t)hq * n_q + i) * kD)[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// dq[i][hq][:] = bf16(scale * dq_acc[hq][i][:]).  One warp per (row, head).
+__global__ void bwd_convert(const float* __restrict__ dq_acc, int n_q, int Hq, float scale,
+                            __nv_bfloat16* __restrict__ dq) {
+  const int w = (blockIdx.x * blockDim.x + threadIdx.x) / 32, lane = threadIdx.x % 32;
+  if (w >= n_q * Hq) return;
+  const int i = w / Hq, hq = w % Hq;
+  const float4 x = reinterpret_cast<const float4*>(dq_acc + ((size_t)hq * n_q + i) * kD)[lane];
+  uint2 out;
+  out.x = pack_bf16x2(x.x * scale, x.y * scale);
+  out.y = pack_bf16x2(x.z * scale, x.w * scale);
+  *reinterpret_cast<uint2*>(dq + ((size_t)i * Hq + hq) * kD + lane * 4) = out;
+}
+
+}  // namespace
+
+cudaError_t launch_attn_bwd_tc(const AttnArgs& a, cudaStream_t st) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(attn_bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  float* Dbuf = reinterpret_cast<float*>(a.ws);
+  float* dq_acc = reinterpret_cast<float*>(reinterpret_cast<char*>(a.ws) +
+                                           align_up((size_t)a.g.Hq * a.n_q * 4, 256));
+  const int warps = a.n_q * a.g.Hq;
+  bwd_prep<<<(warps + 7) / 8, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(a.o),
+                                            reinterpret_cast<const __nv_bfloat16*>(a.dout), a.n_q, a.g.Hq, Dbuf,
+                                            dq_acc);
+  CUtensorMap tq, tdo, tk, tv;
+  if (!make_tmap_heads(&tq, a.q, a.n_q, a.g.Hq, kHalf) || !make_tmap_heads(&tdo, a.dout, a.n_q, a.g.Hq, kHalf) ||
+      !make_tmap_rows(&tk, a.kv.k, kv_rows(a)) || !make_tmap_rows(&tv, a.kv.v, kv_rows(a)))
+    return cudaErrorInvalidValue;
+  BwdParams p;
+  p.sel = a.sel;
+  p.sel_count = a.sel_count;
+  p.table = a.kv.table;
+  p.lse = a.lse_in;
+  p.Dbuf = Dbuf;
+  p.dq_acc = dq_acc;
+  p.dk_pool = a.dk_pool;
+  p.dv_pool = a.dv_pool;
+  p.err = a.err;
+  p.max_sel = a.max_sel;
+  p.n_q = a.n_q;
+  p.Hq = a.g.Hq;
+  p.G = a.g.G;
+  p.Hkv = a.g.Hkv;
+  p.num_phys = a.g.num_phys;
+  p.max_logical = a.g.max_logical;
+  p.n_tiles = (a.n_q + kTile - 1) / kTile;
+  p.q_start = a.q_start;
+  p.scale = a.scale;
+  p.scale_log2 = a.scale * kLog2e;
+  p.staged = a.kv.staged;
+  p.stage_h0 = a.kv.stage_h0;
+  p.stage_stride = a.kv.stage_stride;
+  dim3 grid(a.max_sel, a.g.Hkv);
+  attn_bwd_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(tq, tdo, tk, tv, p);
+  bwd_convert<<<(warps + 7) / 8, 256, 0, st>>>(dq_acc, a.n_q, a.g.Hq, a.scale,
+                                               reinterpret_cast<__nv_bfloat16*>(a.dq));
+  count_launches(3);
+  return cudaGetLastError();
+}
 
 }  // namespace oomb

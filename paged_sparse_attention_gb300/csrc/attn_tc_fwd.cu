@@ -116,6 +116,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tq);
       tma_prefetch_desc(&tk);
       tma_prefetch_desc(&tv);
+      // every selection entry must name an existing page of this chunk's view
+      const int nvis = (int)((p.q_start + p.n_q + kTile - 1) / kTile);
+      for (int e = 0; e < count; ++e) {
+        const int pe = p.sel[(size_t)h * p.max_sel + e];
+        if (pe < 0 || pe >= nvis) {
+          atomicOr(p.err, OOMB_DEVERR_SEL);
+          break;
+        }
+      }
       mbar_arrive_expect_tx(&bar->q_full, kTileBytes);
       tma_load_3d(sQ, &tq, &bar->q_full, 0, hq, t * kTile);
       tma_load_3d(sQ + kHalfBytes, &tq, &bar->q_full, 64, hq, t * kTile);

@@ -22,14 +22,14 @@ constexpr float kLn2 = 0.6931471805599453f;
 //
 // K-major operand (rows = M or N, 128-wide K split over the two boxes): the
 // 16-wide K step kk starts in box kk/4 at byte (kk%4)*32 of the row.
-__device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile_saddr, int kk) {
-  return smem_desc(tile_saddr + (uint32_t)(kk >> 2) * kHalfBytes + (uint32_t)(kk & 3) * 32u, 16, 1024,
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile_saddr, int kk, uint32_t box_bytes = kHalfBytes) {
+  return smem_desc(tile_saddr + (uint32_t)(kk >> 2) * box_bytes + (uint32_t)(kk & 3) * 32u, 16, 1024,
                    kSwizzle128B);
 }
 // MN-major operand (rows = K, 128-wide M/N split over the two boxes, LBO = box
 // stride): the 16-row K step kk starts at row 16*kk.
-__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile_saddr, int kk) {
-  return smem_desc(tile_saddr + (uint32_t)kk * 2048u, kHalfBytes, 1024, kSwizzle128B);
+__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile_saddr, int kk, uint32_t box_bytes = kHalfBytes) {
+  return smem_desc(tile_saddr + (uint32_t)kk * 2048u, box_bytes, 1024, kSwizzle128B);
 }
 
 // Byte offset of element (row, col) of a 128x128 bf16 tile stored in the layout above
@@ -69,14 +69,14 @@ inline bool make_tmap_rows(CUtensorMap* m, const void* base, uint64_t rows) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 3-D map over a token-major [n, H, 128] bf16 tensor: box = 128 tokens of one head,
-// 64 columns; tokens beyond n read as zero.
-inline bool make_tmap_heads(CUtensorMap* m, const void* base, int n, int H) {
+// 3-D map over a token-major [n, H, 128] bf16 tensor: box = `rows` tokens of one
+// head, 64 columns; tokens beyond n read as zero.
+inline bool make_tmap_heads(CUtensorMap* m, const void* base, int n, int H, int rows = kTile) {
   auto enc = tmap_encoder();
   if (!enc) return false;
   cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)n};
   cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)H * kD * 2};
-  cuuint32_t box[3] = {64, 1, kTile};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)rows};
   cuuint32_t es[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
