@@ -145,6 +145,32 @@ OOMB_API oomb_status oomb_page_select(oomb_pool* pool, const void* q, int64_t q_
                              int32_t* sel, int32_t* sel_count, int max_sel, void* workspace, size_t ws_bytes,
                              void* stream);
 
+/* oomb_page_select for callers that cannot allocate device memory.  The pages
+ * describe no counterpart: this is a property of the library, not of the method.
+ * Identical selection to oomb_page_select, but the scratch it needs comes from a
+ * static device array of 4 MiB inside the library (held by every GPU that loads
+ * the library until the process exits) instead of a caller workspace.  Meant for
+ * callers that cannot call cudaMalloc: a framework that owns all device memory
+ * through its own pool, a steady-state loop where allocation (which can
+ * synchronize the device or fail under memory pressure) is forbidden, or a C host
+ * with no allocator of its own.  The caller still passes q, sel and sel_count.
+ *  - Limit: returns OOMB_ERR_WORKSPACE when oomb_workspace_size(pool,
+ *    OOMB_OP_SELECT, n_q) exceeds 4 MiB (e.g. more than 262,144 logical pages at
+ *    4 KV heads x head_dim 128).
+ *  - Set-up: the first call on a device looks up the array's device address with
+ *    cudaGetSymbolAddress while that device is current; make that first call
+ *    before any stream capture.
+ *  - Sharing: every call on a device uses the same array and leaves its contents
+ *    behind; nothing in it needs to start at zero.  Calls that overlap on the GPU
+ *    (different streams, or different host threads) race on the array: order
+ *    them on one stream.
+ *  - Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
+ * Errors: those of oomb_page_select, plus WORKSPACE (above the limit) and CUDA
+ * (set-up failed). */
+OOMB_API oomb_status oomb_page_select_noalloc(oomb_pool* pool, const void* q, int64_t q_start, int n_q, int top_k,
+                                              int n_sink, int32_t* sel, int32_t* sel_count, int max_sel,
+                                              void* stream);
+
 /* Chunk attention forward.  For query head hq and row i (absolute position
  * q_start+i): keys = every token of the selected pages of KV head hq/G with
  * position <= q_start+i; O_i = softmax(scale * q_i . k_j) V and

@@ -74,6 +74,7 @@ def load(path: str = LIB_PATH) -> C.CDLL:
         "oomb_status_str": (C.c_char_p, [i32]),
         "oomb_uses_tensor_cores": (i32, [vp]),
         "oomb_launch_count": (C.c_uint64, []),
+        "oomb_page_select_noalloc": (i32, [vp, vp, i64, i32, i32, i32, vp, vp, i32, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -188,3 +189,12 @@ def oomb_uses_tensor_cores(pool: int) -> bool:
 
 def oomb_launch_count() -> int:
     return int(load().oomb_launch_count())
+
+
+def oomb_page_select_noalloc(pool: int, q, q_start: int, top_k: int, n_sink: int, sel, sel_count,
+                             n_q: Optional[int] = None, stream=None) -> None:
+    """oomb_page_select with the library's static scratch instead of a workspace."""
+    n = q.shape[0] if n_q is None else n_q
+    _ok("oomb_page_select_noalloc", load().oomb_page_select_noalloc(pool, _ptr(q), q_start, n, top_k, n_sink,
+                                                                    _ptr(sel), _ptr(sel_count), sel.shape[-1],
+                                                                    _stream(stream)))
