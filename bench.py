@@ -94,7 +94,7 @@ class ClockSampler:
 class Step:
     """Device buffers and the per-chunk call sequence of one benchmark step."""
 
-    def __init__(self, w, dev, seed_offset=0):
+    def __init__(self, w, dev, host_inputs=False):
         import torch
 
         import paged_sparse_attention_gb300 as L
@@ -104,13 +104,22 @@ class Step:
         self.L, self.torch, self.w, self.dev = L, torch, w, dev
         self.scale = 1.0 / math.sqrt(w.head_dim)
         order = synth.page_order(w)
+        self.offload = bool(w.offload)
         self.pool = PagedKVPool(w.n_q_heads, w.n_kv_heads, w.head_dim, w.page, w.num_phys, w.n_pages,
-                                w.torch_dtype, dev, page_order=order)
+                                w.torch_dtype, dev, page_order=order, offload=self.offload,
+                                stage_max_sel=w.max_sel if self.offload else 0)
         plants = synth.PlantTable(w) if w.plants > 0 else None
-        # inputs generated on the device, per chunk (seeded), resident for the whole run
-        self.chunks = []
+        # inputs generated per chunk (seeded) on the device -- or on the host and uploaded,
+        # keeping the host copies, when a test needs the same tensors for the oracle --
+        # and resident for the whole run
+        self.chunks, self.host_chunks = [], []
         for c in range(w.n_chunks):
-            self.chunks.append(synth.make_chunk(w, c, device=dev, plants=plants))
+            if host_inputs:
+                hc = synth.make_chunk(w, c, device="cpu", plants=plants)
+                self.host_chunks.append(hc)
+                self.chunks.append({k: v.to(dev) for k, v in hc.items()})
+            else:
+                self.chunks.append(synth.make_chunk(w, c, device=dev, plants=plants))
         C = w.chunk
         self.ws_sel = self.pool.workspace(L.OOMB_OP_SELECT, C)
         self.ws_bwd = self.pool.workspace(L.OOMB_OP_BWD, C)
@@ -120,10 +129,12 @@ class Step:
         self.lse = torch.empty((w.n_q_heads, C), dtype=torch.float32, device=dev)
         self.dq = [torch.empty_like(ch["q"]) for ch in self.chunks]
         self.fwd_events, self.bwd_events = [], []
+        self.side = torch.cuda.Stream(device=dev) if self.offload else None
 
     def run(self, record=False):
+        if self.offload:
+            return self.run_offload(record)
         L, w, h = self.L, self.w, self.pool.handle
-        torch = self.torch
         L.oomb_pool_reset(h)
         for c, ch in enumerate(self.chunks):
             start, n = w.chunk_bounds(c)
@@ -131,18 +142,77 @@ class Step:
             L.oomb_page_select(h, ch["q"], start, w.top_k, w.n_sink, self.sel[c], self.cnt[c], self.ws_sel)
             self._fwd(c, ch, start, n, record)
         for c in range(w.n_chunks - 1, -1, -1):
-            ch = self.chunks[c]
             start, n = w.chunk_bounds(c)
-            self._fwd(c, ch, start, n, record)  # recompute (activations are not kept)
-            if record:
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record()
-            lse = self.lse if n == w.chunk else self.lse_tail(n)
-            L.oomb_chunk_attn_bwd(h, ch["q"], self.o[:n], ch["do"], lse, start, self.sel[c], self.cnt[c],
-                                  self.scale, self.dq[c], self.ws_bwd)
-            if record:
-                e1.record()
-                self.bwd_events.append((e0, e1, c))
+            self._fwd(c, self.chunks[c], start, n, record)  # recompute (activations are not kept)
+            self._bwd(c, self.chunks[c], start, n, record)
+
+    def run_offload(self, record=False):
+        """K/V pools in pinned host memory.  The side stream gathers the selected pages
+        of the next chunk into the other staging buffer while the main stream runs the
+        current chunk's attention (forward sweep: chunk c+1 is appended and selected
+        before chunk c's forward; reverse sweep: chunk c-1 is gathered during chunk c)."""
+        L, w, h, torch = self.L, self.w, self.pool.handle, self.torch
+        main, side = torch.cuda.current_stream(self.dev), self.side
+        S = w.n_chunks
+        ev = lambda: torch.cuda.Event()  # noqa: E731
+        L.oomb_pool_reset(h)
+
+        def append_select(c):
+            start, n = w.chunk_bounds(c)
+            ch = self.chunks[c]
+            L.oomb_kv_append(h, ch["k"], ch["v"], start)
+            L.oomb_page_select(h, ch["q"], start, w.top_k, w.n_sink, self.sel[c], self.cnt[c], self.ws_sel)
+
+        def prefetch(c, after):
+            for e in after:
+                side.wait_event(e)
+            L.oomb_prefetch(h, self.sel[c], self.cnt[c], c % 2, stream=side)
+            done = ev()
+            done.record(side)
+            return done
+
+        # forward sweep
+        append_select(0)
+        sel_ev = ev()
+        sel_ev.record(main)
+        pf = {0: prefetch(0, [sel_ev])}
+        used = {}
+        for c in range(S):
+            if c + 1 < S:
+                append_select(c + 1)
+                e = ev()
+                e.record(main)
+                pf[c + 1] = prefetch(c + 1, [e] + ([used[c - 1]] if c - 1 in used else []))
+            main.wait_event(pf[c])
+            L.oomb_pool_set_stage(h, c % 2)
+            start, n = w.chunk_bounds(c)
+            self._fwd(c, self.chunks[c], start, n, record)
+            used[c] = ev()
+            used[c].record(main)
+        # reverse sweep
+        pf = {S - 1: prefetch(S - 1, [used[S - 1]])}
+        for c in range(S - 1, -1, -1):
+            if c - 1 >= 0:
+                pf[c - 1] = prefetch(c - 1, [used[c + 1]] if c + 1 < S else [used[S - 1]])
+            main.wait_event(pf[c])
+            L.oomb_pool_set_stage(h, c % 2)
+            start, n = w.chunk_bounds(c)
+            self._fwd(c, self.chunks[c], start, n, record)
+            self._bwd(c, self.chunks[c], start, n, record)
+            used[c] = ev()
+            used[c].record(main)
+
+    def _bwd(self, c, ch, start, n, record):
+        L, torch, w = self.L, self.torch, self.w
+        if record:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+        lse = self.lse if n == w.chunk else self.lse_tail(n)
+        L.oomb_chunk_attn_bwd(self.pool.handle, ch["q"], self.o[:n], ch["do"], lse, start, self.sel[c],
+                              self.cnt[c], self.scale, self.dq[c], self.ws_bwd)
+        if record:
+            e1.record()
+            self.bwd_events.append((e0, e1, c))
 
     def _fwd(self, c, ch, start, n, record):
         L, torch = self.L, self.torch

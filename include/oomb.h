@@ -226,6 +226,10 @@ OOMB_API int oomb_pool_free_pages(const oomb_pool* pool);
 
 OOMB_API const char* oomb_status_str(oomb_status s);
 
+/* Text of the last CUDA runtime error a call of this library returned
+ * OOMB_ERR_CUDA for on the calling host thread ("" if none). */
+OOMB_API const char* oomb_last_cuda_error(void);
+
 /* Kernels this library has launched since it was loaded (all pools, all devices). */
 OOMB_API uint64_t oomb_launch_count(void);
 

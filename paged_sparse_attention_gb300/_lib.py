@@ -75,6 +75,7 @@ def load(path: str = LIB_PATH) -> C.CDLL:
         "oomb_uses_tensor_cores": (i32, [vp]),
         "oomb_launch_count": (C.c_uint64, []),
         "oomb_page_select_noalloc": (i32, [vp, vp, i64, i32, i32, i32, vp, vp, i32, vp]),
+        "oomb_last_cuda_error": (C.c_char_p, []),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -99,7 +100,10 @@ def _stream(stream) -> Optional[int]:
 
 def _ok(name: str, st: int):
     if st != 0:
-        raise OombError(name, st, load().oomb_status_str(st).decode())
+        detail = load().oomb_status_str(st).decode()
+        if st == 7:
+            detail += ": " + load().oomb_last_cuda_error().decode()
+        raise OombError(name, st, detail)
 
 
 # ---------------------------------------------------------------- entry points

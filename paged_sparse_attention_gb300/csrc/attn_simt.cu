@@ -381,9 +381,8 @@ cudaError_t bwd_simt(const AttnArgs& a, cudaStream_t st) {
 }  // namespace
 
 size_t bwd_workspace_bytes(const Geometry& g, int n_q) {
-  size_t b = align_up((size_t)g.Hq * n_q * 4, 256);  // D
-  if (tc_supported(g)) b += align_up((size_t)g.Hq * n_q * g.d * 4, 256);  // fp32 dQ accumulator
-  return b;
+  const size_t simt = align_up((size_t)g.Hq * n_q * 4, 256);  // D
+  return tc_supported(g) ? bwd_tc_workspace_bytes(g, n_q) : simt;
 }
 
 cudaError_t launch_attn_fwd_simt(const AttnArgs& a, cudaStream_t st) {

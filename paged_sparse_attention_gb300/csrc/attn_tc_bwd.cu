@@ -48,13 +48,13 @@ struct BwdParams {
   const int32_t* sel;
   const int32_t* sel_count;
   const int32_t* table;
-  const float* lse;
-  const float* Dbuf;
+  const float* lse2;  // [Hq, n_pad] LSE * log2(e), +inf on padded rows
+  const float* Dbuf;  // [Hq, n_pad] rowsum(dO * O), 0 on padded rows
   float* dq_acc;
   float* dk_pool;
   float* dv_pool;
   uint32_t* err;
-  int max_sel, n_q, Hq, G, Hkv, num_phys, max_logical, n_tiles;
+  int max_sel, n_q, n_pad, Hq, G, Hkv, num_phys, max_logical, n_tiles;
   int64_t q_start;
   float scale, scale_log2;
   int staged, stage_h0, stage_stride;
@@ -151,34 +151,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load_2d(sm + kOffV, &tv, &bar->kv_full, 0, row);
       tma_load_2d(sm + kOffV + kHalfBytes, &tv, &bar->kv_full, 64, row);
     }
-    bool ok = true;
     int v = 0;
-    for (; v < 2 * n_steps; ++v) {
-      const int slot = v % kRing;
-      if (v >= kRing) {
-        if (lane == 0) ok = mbar_wait(&bar->hs_empty[slot], ((v / kRing) - 1) & 1, p.err, abort);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-      }
-      const int u = v >> 1, hh = v & 1;
-      const int t = t0 + u / p.G, g = u % p.G;
-      const int hq = h * p.G + g;
-      const int q0 = t * kTile + hh * kHalf;
-      float* vs = vec + slot * 2 * kHalf;
-      for (int i = lane; i < kHalf; i += 32) {
-        const int qi = q0 + i;
-        const bool valid = qi < p.n_q;
-        vs[i] = valid ? p.lse[(size_t)hq * p.n_q + qi] * kLog2e : INFINITY;
-        vs[kHalf + i] = valid ? p.Dbuf[(size_t)hq * p.n_q + qi] : 0.f;
-      }
-      __syncwarp();
-      if (lane == 0) {
+    if (lane == 0) {
+      for (; v < 2 * n_steps; ++v) {
+        const int slot = v % kRing;
+        if (v >= kRing && !mbar_wait(&bar->hs_empty[slot], ((v / kRing) - 1) & 1, p.err, abort)) break;
+        const int u = v >> 1, hh = v & 1;
+        const int t = t0 + u / p.G, g = u % p.G;
+        const int hq = h * p.G + g;
+        const int q0 = t * kTile + hh * kHalf;
         uint8_t* dst = sm + kOffRing + slot * 2 * kHalfTile;
-        mbar_arrive_expect_tx(&bar->hs_full[slot], 2 * kHalfTile);
+        float* vs = vec + slot * 2 * kHalf;
+        mbar_arrive_expect_tx(&bar->hs_full[slot], 2 * kHalfTile + 2 * kHalf * 4);
         tma_load_3d(dst, &tq, &bar->hs_full[slot], 0, hq, q0);
         tma_load_3d(dst + kHalfBox, &tq, &bar->hs_full[slot], 64, hq, q0);
         tma_load_3d(dst + kHalfTile, &tdo, &bar->hs_full[slot], 0, hq, q0);
         tma_load_3d(dst + kHalfTile + kHalfBox, &tdo, &bar->hs_full[slot], 64, hq, q0);
+        // LSE * log2(e) and D of the 64 rows (padded rows hold +inf and 0)
+        bulk_load(vs, p.lse2 + (size_t)hq * p.n_pad + q0, kHalf * 4, &bar->hs_full[slot]);
+        bulk_load(vs + kHalf, p.Dbuf + (size_t)hq * p.n_pad + q0, kHalf * 4, &bar->hs_full[slot]);
       }
     }
     if (lane == 0) {  // drain the copies still in flight before the CTA may exit
@@ -195,45 +186,52 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t aK = smem_u32(sm + kOffK), aV = smem_u32(sm + kOffV);
       bool ok = mbar_wait(&bar->kv_full, 0, p.err, abort);
       bool first_acc = true;
+      // S^T, dP^T of half-step v = 2u + hh into the half's TMEM region
+      auto issue_sdp = [&](int u, int hh) -> bool {
+        const int v = 2 * u + hh, slot = v % kRing;
+        if (!mbar_wait(&bar->hs_full[slot], (v / kRing) & 1, p.err, abort)) return false;
+        if (u > 0 && !mbar_wait(&bar->dq_free[hh], (u - 1) & 1, p.err, abort)) return false;  // dQ^T read out
+        tc_fence_after();
+        const uint32_t aQ = smem_u32(sm + kOffRing + slot * 2 * kHalfTile);
+        const uint32_t adO = aQ + kHalfTile;
+        const uint32_t tS = tmem + hh * 128;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) mma_ss(tS, desc_kmajor(aK, kk), desc_kmajor(aQ, kk, kHalfBox), id_s, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tS + 64, desc_kmajor(aV, kk), desc_kmajor(adO, kk, kHalfBox), id_s, kk > 0);
+        mma_commit(&bar->s_full[hh]);
+        return true;
+      };
+      // dV += P^T dO, dK += dS^T Q, dQ^T = K^T dS^T once the half's softmax is done
+      auto issue_acc = [&](int u, int hh) -> bool {
+        const int v = 2 * u + hh, slot = v % kRing;
+        if (!mbar_wait(&bar->p_full[hh], u & 1, p.err, abort)) return false;
+        tc_fence_after();
+        const uint32_t aQ = smem_u32(sm + kOffRing + slot * 2 * kHalfTile);
+        const uint32_t adO = aQ + kHalfTile;
+        const uint32_t tS = tmem + hh * 128;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          mma_ts(tmem + 256, tS + kk * 8, desc_mnmajor(adO, kk, kHalfBox), id_acc, first_acc ? 0u : 1u);
+          mma_ts(tmem + 384, tS + 32 + kk * 8, desc_mnmajor(aQ, kk, kHalfBox), id_acc, first_acc ? 0u : 1u);
+          first_acc = false;
+        }
+        mma_commit(&bar->hs_empty[slot]);
+        const uint32_t adS = smem_u32(sm + kOffDS + hh * kHalfTile);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tS + 64, desc_mnmajor(aK, kk), desc_mnmajor(adS, kk, kHalfBox), id_dq, kk > 0);
+        mma_commit(&bar->dq_full[hh]);
+        return true;
+      };
+      // half b's softmax overlaps the next step's S/dP of half a, and vice versa
+      if (ok) ok = issue_sdp(0, 0) && issue_sdp(0, 1);
       for (int u = 0; ok && u < n_steps; ++u) {
-        for (int hh = 0; hh < 2 && ok; ++hh) {
-          const int v = 2 * u + hh, slot = v % kRing;
-          ok = mbar_wait(&bar->hs_full[slot], (v / kRing) & 1, p.err, abort);
-          if (ok && u > 0) ok = mbar_wait(&bar->dq_free[hh], (u - 1) & 1, p.err, abort);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t aQ = smem_u32(sm + kOffRing + slot * 2 * kHalfTile);
-          const uint32_t adO = aQ + kHalfTile;
-          const uint32_t tS = tmem + hh * 128;
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ss(tS, desc_kmajor(aK, kk), desc_kmajor(aQ, kk, kHalfBox), id_s, kk > 0);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ss(tS + 64, desc_kmajor(aV, kk), desc_kmajor(adO, kk, kHalfBox), id_s, kk > 0);
-          mma_commit(&bar->s_full[hh]);
-        }
-        for (int hh = 0; hh < 2 && ok; ++hh) {
-          const int v = 2 * u + hh, slot = v % kRing;
-          ok = mbar_wait(&bar->p_full[hh], u & 1, p.err, abort);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t aQ = smem_u32(sm + kOffRing + slot * 2 * kHalfTile);
-          const uint32_t adO = aQ + kHalfTile;
-          const uint32_t tS = tmem + hh * 128;
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            mma_ts(tmem + 256, tS + kk * 8, desc_mnmajor(adO, kk, kHalfBox), id_acc, first_acc ? 0u : 1u);
-            mma_ts(tmem + 384, tS + 32 + kk * 8, desc_mnmajor(aQ, kk, kHalfBox), id_acc, first_acc ? 0u : 1u);
-            first_acc = false;
-          }
-          mma_commit(&bar->hs_empty[slot]);
-          const uint32_t adS = smem_u32(sm + kOffDS + hh * kHalfTile);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ss(tS + 64, desc_mnmajor(aK, kk), desc_mnmajor(adS, kk, kHalfBox), id_dq, kk > 0);
-          mma_commit(&bar->dq_full[hh]);
-        }
+        ok = issue_acc(u, 0);
+        if (ok && u + 1 < n_steps) ok = issue_sdp(u + 1, 0);
+        if (ok) ok = issue_acc(u, 1);
+        if (ok && u + 1 < n_steps) ok = issue_sdp(u + 1, 1);
       }
       mma_commit(&bar->acc_full);
       mbar_wait(&bar->acc_full, 0, p.err, nullptr);
@@ -261,32 +259,42 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(base + 96, *reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
           tmem_wait_ld();
         }
-        const float* vs = vec + slot * 2 * kHalf;
-        uint32_t pk[32], dk[32];
+        const float4* vs4 = reinterpret_cast<const float4*>(vec + slot * 2 * kHalf);  // lse2[64], D[64]
         const int qbase = hh * kHalf;  // query row (within the tile) of column 0
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          float pr[2], dsr[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int i = 2 * c + e;
-            float pv = exp2f(fmaf(__uint_as_float(sr[i]), p.scale_log2, -vs[i]));
-            if (diag && j > qbase + i) pv = 0.f;
-            pr[e] = pv;
-            dsr[e] = pv * (__uint_as_float(dr[i]) - vs[kHalf + i]);
-          }
-          pk[c] = pack_bf16x2(pr[0], pr[1]);
-          dk[c] = pack_bf16x2(dsr[0], dsr[1]);
-        }
+        const bool masked = diag && (j > qbase);  // some column of this half is in the key's future
         const uint32_t base = tmem + lane_off + hh * 128;
-        tmem_st32(base + 0, pk);
-        tmem_st32(base + 32, dk);
-        // dS^T row j (64 query columns) into the swizzled B-operand tile of the dQ^T MMA
         uint8_t* drow = sm + kOffDS + hh * kHalfTile + j * 128;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint4 w = make_uint4(dk[4 * c], dk[4 * c + 1], dk[4 * c + 2], dk[4 * c + 3]);
-          *reinterpret_cast<uint4*>(drow + ((c ^ (j & 7)) * 16)) = w;
+        for (int part = 0; part < 2; ++part) {  // 32 query columns at a time
+          uint32_t pk[16], dk[16];
+#pragma unroll
+          for (int c4 = 0; c4 < 8; ++c4) {
+            const float4 L = vs4[part * 8 + c4], Dv = vs4[16 + part * 8 + c4];
+            const float l4[4] = {L.x, L.y, L.z, L.w}, d4[4] = {Dv.x, Dv.y, Dv.z, Dv.w};
+            float pr[4], dsr[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int i = part * 32 + 4 * c4 + e;
+              float pv = ex2_approx(fmaf(__uint_as_float(sr[i]), p.scale_log2, -l4[e]));
+              if (masked && j > qbase + i) pv = 0.f;
+              pr[e] = pv;
+              dsr[e] = pv * (__uint_as_float(dr[i]) - d4[e]);
+            }
+            pk[2 * c4] = pack_bf16x2(pr[0], pr[1]);
+            pk[2 * c4 + 1] = pack_bf16x2(pr[2], pr[3]);
+            dk[2 * c4] = pack_bf16x2(dsr[0], dsr[1]);
+            dk[2 * c4 + 1] = pack_bf16x2(dsr[2], dsr[3]);
+          }
+          // the whole half was already loaded into registers, so its TMEM columns may be overwritten
+          tmem_st16(base + part * 16, pk);
+          tmem_st16(base + 32 + part * 16, dk);
+          // dS^T row j, query columns [32 part, 32 part + 32): four 16-byte chunks of the swizzled tile
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int chunk = part * 4 + c;
+            uint4 w = make_uint4(dk[4 * c], dk[4 * c + 1], dk[4 * c + 2], dk[4 * c + 3]);
+            *reinterpret_cast<uint4*>(drow + ((chunk ^ (j & 7)) * 16)) = w;
+          }
         }
         tmem_wait_st();
         fence_proxy_async_smem();
@@ -376,12 +384,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// D = rowsum(dO * O) per (row, head); dq_acc rows zeroed.  One warp per (row, head).
-__global__ void bwd_prep(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout, int n_q,
-                         int Hq, float* __restrict__ Dbuf, float* __restrict__ dq_acc) {
+// Per (row, head) of the padded range: D = rowsum(dO * O) and LSE * log2(e) into
+// [Hq, n_pad] buffers (rows past n_q: D = 0, LSE = +inf so that P = 0), and the
+// row of the fp32 dQ accumulator zeroed.  One warp per (row, head).
+__global__ void bwd_prep(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
+                         const float* __restrict__ lse, int n_q, int n_pad, int Hq, float* __restrict__ Dbuf,
+                         float* __restrict__ lse2, float* __restrict__ dq_acc) {
   const int w = (blockIdx.x * blockDim.x + threadIdx.x) / 32, lane = threadIdx.x % 32;
-  if (w >= n_q * Hq) return;
+  if (w >= n_pad * Hq) return;
   const int i = w / Hq, hq = w % Hq;
+  if (i >= n_q) {
+    if (lane == 0) {
+      Dbuf[(size_t)hq * n_pad + i] = 0.f;
+      lse2[(size_t)hq * n_pad + i] = INFINITY;
+    }
+    return;
+  }
   const size_t off = ((size_t)i * Hq + hq) * kD + lane * 4;
   const uint2 a = *reinterpret_cast<const uint2*>(o + off);
   const uint2 b = *reinterpret_cast<const uint2*>(dout + off);
@@ -395,7 +413,10 @@ __global__ void bwd_prep(const __nv_bfloat16* __restrict__ o, const __nv_bfloat1
   }
 #pragma unroll
   for (int off2 = 16; off2 > 0; off2 >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off2);
-  if (lane == 0) Dbuf[(size_t)hq * n_q + i] = s;
+  if (lane == 0) {
+    Dbuf[(size_t)hq * n_pad + i] = s;
+    lse2[(size_t)hq * n_pad + i] = lse[(size_t)hq * n_q + i] * kLog2e;
+  }
   reinterpret_cast<float4*>(dq_acc + ((size_t)hq * n_q + i) * kD)[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
@@ -414,6 +435,11 @@ __global__ void bwd_convert(const float* __restrict__ dq_acc, int n_q, int Hq, f
 
 }  // namespace
 
+size_t bwd_tc_workspace_bytes(const Geometry& g, int n_q) {
+  const size_t n_pad = (size_t)(n_q + kTile - 1) / kTile * kTile;
+  return 2 * align_up((size_t)g.Hq * n_pad * 4, 256) + align_up((size_t)g.Hq * n_q * kD * 4, 256);
+}
+
 cudaError_t launch_attn_bwd_tc(const AttnArgs& a, cudaStream_t st) {
   static bool attr_set = false;
   if (!attr_set) {
@@ -422,13 +448,16 @@ cudaError_t launch_attn_bwd_tc(const AttnArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  float* Dbuf = reinterpret_cast<float*>(a.ws);
-  float* dq_acc = reinterpret_cast<float*>(reinterpret_cast<char*>(a.ws) +
-                                           align_up((size_t)a.g.Hq * a.n_q * 4, 256));
+  const int n_pad = (a.n_q + kTile - 1) / kTile * kTile;
+  char* ws = reinterpret_cast<char*>(a.ws);
+  float* Dbuf = reinterpret_cast<float*>(ws);
+  float* lse2 = reinterpret_cast<float*>(ws + align_up((size_t)a.g.Hq * n_pad * 4, 256));
+  float* dq_acc = reinterpret_cast<float*>(ws + 2 * align_up((size_t)a.g.Hq * n_pad * 4, 256));
   const int warps = a.n_q * a.g.Hq;
-  bwd_prep<<<(warps + 7) / 8, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(a.o),
-                                            reinterpret_cast<const __nv_bfloat16*>(a.dout), a.n_q, a.g.Hq, Dbuf,
-                                            dq_acc);
+  const int warps_pad = n_pad * a.g.Hq;
+  bwd_prep<<<(warps_pad + 7) / 8, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(a.o),
+                                                reinterpret_cast<const __nv_bfloat16*>(a.dout), a.lse_in, a.n_q,
+                                                n_pad, a.g.Hq, Dbuf, lse2, dq_acc);
   CUtensorMap tq, tdo, tk, tv;
   if (!make_tmap_heads(&tq, a.q, a.n_q, a.g.Hq, kHalf) || !make_tmap_heads(&tdo, a.dout, a.n_q, a.g.Hq, kHalf) ||
       !make_tmap_rows(&tk, a.kv.k, kv_rows(a)) || !make_tmap_rows(&tv, a.kv.v, kv_rows(a)))
@@ -437,7 +466,7 @@ cudaError_t launch_attn_bwd_tc(const AttnArgs& a, cudaStream_t st) {
   p.sel = a.sel;
   p.sel_count = a.sel_count;
   p.table = a.kv.table;
-  p.lse = a.lse_in;
+  p.lse2 = lse2;
   p.Dbuf = Dbuf;
   p.dq_acc = dq_acc;
   p.dk_pool = a.dk_pool;
@@ -445,6 +474,7 @@ cudaError_t launch_attn_bwd_tc(const AttnArgs& a, cudaStream_t st) {
   p.err = a.err;
   p.max_sel = a.max_sel;
   p.n_q = a.n_q;
+  p.n_pad = n_pad;
   p.Hq = a.g.Hq;
   p.G = a.g.G;
   p.Hkv = a.g.Hkv;

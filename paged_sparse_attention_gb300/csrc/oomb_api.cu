@@ -29,7 +29,13 @@ namespace {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-oomb_status cuda_status(cudaError_t e) { return e == cudaSuccess ? OOMB_OK : OOMB_ERR_CUDA; }
+thread_local const char* t_last_cuda_error = "";
+
+oomb_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return OOMB_OK;
+  t_last_cuda_error = cudaGetErrorString(e);
+  return OOMB_ERR_CUDA;
+}
 
 Geometry geometry_of(const oomb_pool_desc& d) {
   Geometry g;
@@ -172,6 +178,8 @@ int oomb_page_table_host(const oomb_pool* p, int32_t* out, int n) {
   return m;
 }
 
+const char* oomb_last_cuda_error(void) { return t_last_cuda_error; }
+
 uint64_t oomb_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 int oomb_uses_tensor_cores(const oomb_pool* p) { return p && tc_supported(p->g) ? 1 : 0; }
@@ -190,7 +198,7 @@ oomb_status oomb_kv_append(oomb_pool* p, const void* k, const void* v, int64_t f
   const int n_new = (int)(end_page - first_page);
   if (n_new > (int)p->free_list.size()) return OOMB_ERR_OUT_OF_PAGES;
   cudaError_t e = clear_table_if_dirty(p, (cudaStream_t)stream);
-  if (e != cudaSuccess) return OOMB_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_status(e);
   std::vector<int32_t> newp(n_new);
   for (int i = 0; i < n_new; ++i) {
     newp[i] = p->free_list.back();
@@ -205,7 +213,7 @@ oomb_status oomb_kv_append(oomb_pool* p, const void* k, const void* v, int64_t f
       p->free_list.push_back(newp[i]);
       p->table[first_page + i] = -1;
     }
-    return OOMB_ERR_CUDA;
+    return cuda_status(e);
   }
   p->n_tokens = end;
   return OOMB_OK;
@@ -322,7 +330,7 @@ oomb_status oomb_check(oomb_pool* p, void* stream, uint32_t* bits_out) {
   if (e == cudaSuccess && bits) e = cudaMemset(p->d.error_word, 0, sizeof(uint32_t));
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (bits_out) *bits_out = bits;
-  if (e != cudaSuccess) return OOMB_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_status(e);
   if (bits & OOMB_DEVERR_TIMEOUT) return OOMB_ERR_TIMEOUT;
   return bits ? OOMB_ERR_KERNEL : OOMB_OK;
 }

@@ -68,6 +68,7 @@ cudaError_t launch_attn_bwd_simt(const AttnArgs& a, cudaStream_t st);
 bool tc_supported(const Geometry& g);
 cudaError_t launch_attn_fwd_tc(const AttnArgs& a, cudaStream_t st);
 cudaError_t launch_attn_bwd_tc(const AttnArgs& a, cudaStream_t st);
+size_t bwd_tc_workspace_bytes(const Geometry& g, int n_q);
 
 cudaError_t launch_prefetch(const Geometry& g, const void* k_pool, const void* v_pool, const int32_t* table,
                             const int32_t* sel, const int32_t* sel_count, int max_sel, void* stage_k, void* stage_v,

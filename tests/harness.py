@@ -45,19 +45,33 @@ class GpuSweep:
     """Forward sweep (append, select, forward) then reverse sweep (recompute
     forward, backward) through the C ABI.  ``sel_override`` feeds given
     selections to the attention calls (the GPU selection is still computed and
-    kept in ``gpu_sel``)."""
+    kept in ``gpu_sel``).  With ``offload`` the K/V pools live in pinned host
+    memory and every chunk's selected pages are prefetched on a side stream into
+    the staging buffer of its parity before its attention calls."""
 
     def __init__(self, w: synth.Workload, chunks, order, dev="cuda", sel_override=None, scale=None,
-                 num_phys: Optional[int] = None):
+                 num_phys: Optional[int] = None, offload: bool = False):
         self.w = w
         self.dev = torch.device(dev)
         self.scale = 1.0 / math.sqrt(w.head_dim) if scale is None else scale
         n_phys = len(order) if num_phys is None else num_phys
-        self.pool = PagedKVPool(w.n_q_heads, w.n_kv_heads, w.head_dim, w.page, n_phys, w.n_pages,
-                                w.torch_dtype, self.dev, page_order=torch.as_tensor(order, dtype=torch.int32))
         max_sel = w.max_sel if sel_override is None else max(w.max_sel, max(max(len(s) for s in so)
                                                                                for so in sel_override))
         self.max_sel = max_sel
+        self.pool = PagedKVPool(w.n_q_heads, w.n_kv_heads, w.head_dim, w.page, n_phys, w.n_pages,
+                                w.torch_dtype, self.dev, page_order=torch.as_tensor(order, dtype=torch.int32),
+                                offload=offload, stage_max_sel=max_sel if offload else 0)
+        side = torch.cuda.Stream(device=self.dev) if offload else None
+        main = torch.cuda.current_stream(self.dev)
+
+        def stage(c, sel, cnt):
+            """Prefetch chunk c's selected pages on the side stream; main waits for them."""
+            if not offload:
+                return
+            side.wait_stream(main)  # selection (and the chunk's own pages) written
+            L.oomb_prefetch(self.pool.handle, sel, cnt, c % 2, stream=side)
+            main.wait_stream(side)
+            L.oomb_pool_set_stage(self.pool.handle, c % 2)
         ws_sel = self.pool.workspace(L.OOMB_OP_SELECT, w.chunk)
         ws_bwd = self.pool.workspace(L.OOMB_OP_BWD, w.chunk)
         h = self.pool.handle
@@ -74,6 +88,7 @@ class GpuSweep:
             self.gpu_sel.append([sel[i, : int(cnt[i])].cpu().numpy() for i in range(w.n_kv_heads)])
             if sel_override is not None:
                 sel, cnt = pad_sel(sel_override[c], max_sel, self.dev)
+            stage(c, sel, cnt)
             o = torch.empty_like(g["q"])
             lse = torch.empty(w.n_q_heads, n, dtype=torch.float32, device=self.dev)
             L.oomb_chunk_attn_fwd(h, g["q"], start, sel, cnt, self.scale, o, lse)
@@ -84,6 +99,7 @@ class GpuSweep:
         for c in range(len(chunks) - 1, -1, -1):
             start, n = w.chunk_bounds(c)
             g = dev_chunks[c]
+            stage(c, g["sel"], g["cnt"])
             o = torch.empty_like(g["q"])
             lse = torch.empty(w.n_q_heads, n, dtype=torch.float32, device=self.dev)
             L.oomb_chunk_attn_fwd(h, g["q"], start, g["sel"], g["cnt"], self.scale, o, lse)  # recompute
