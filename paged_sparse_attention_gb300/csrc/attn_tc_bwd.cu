@@ -22,13 +22,15 @@
 //                atomics.
 //   bwd_convert  dq = bf16(scale * dQ accumulator), token-major.
 //
-// Warp roles of bwd_main (320 threads):
-//   warp 0     TMA producer (K, V once; then a ring of Q/dO half tiles + LSE/D)
-//   warp 1     TMEM owner and MMA issuer
-//   warps 2-5  softmax: thread == key row (TMEM lane); epilogue for dK/dV
-//   warps 6-9  dQ read-out: thread == head-dim column (TMEM lane of dQ^T)
-// TMEM columns: half a [0,128), half b [128,256): S^T [0,64) dP^T [64,128), then
-// P^T [0,32) dS^T [32,64) dQ^T [64,128); dV [256,384); dK [384,512).
+// Warp roles of bwd_main (448 threads):
+//   warp 0      TMA producer (K, V once; then a ring of Q/dO half tiles + LSE/D)
+//   warp 1      TMEM owner and MMA issuer
+//   warps 2-9   softmax: two warps per TMEM lane quarter (thread == key row), each
+//               owning 32 of the half tile's 64 query columns; epilogue for dK/dV
+//   warps 10-13 dQ read-out: thread == head-dim column (TMEM lane of dQ^T)
+// TMEM columns: half a [0,128), half b [128,256): S^T [0,64) dP^T [64,128); after the
+// softmax, query columns [32c, 32c+32) hold P^T packed in [32c, 32c+16) and dS^T
+// packed in [32c+16, 32c+32), and dQ^T overwrites [64,128); dV [256,384); dK [384,512).
 #include "tc_common.cuh"
 
 namespace oomb {
@@ -40,7 +42,8 @@ constexpr int kRing = 3;
 constexpr int kHalf = 64;
 constexpr uint32_t kHalfTile = kHalf * kD * 2;  // 16 KB: one 64-row half tile (two 8 KB boxes)
 constexpr uint32_t kHalfBox = kHalfTile / 2;
-constexpr int kThreads = 320;
+constexpr int kThreads = 448;
+constexpr int kSoftmaxThreads = 256;
 constexpr int kPieceRows = 16;                   // dQ rows per bulk reduce
 constexpr uint32_t kPieceBytes = kPieceRows * kD * 4;
 
@@ -121,7 +124,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar->s_full[i], 1);
-      mbar_init(&bar->p_full[i], 128);
+      mbar_init(&bar->p_full[i], kSoftmaxThreads);
       mbar_init(&bar->dq_full[i], 1);
       mbar_init(&bar->dq_free[i], 128);
     }
@@ -203,7 +206,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&bar->s_full[hh]);
         return true;
       };
-      // dV += P^T dO, dK += dS^T Q, dQ^T = K^T dS^T once the half's softmax is done
+      // dQ^T = K^T dS^T, then dV += P^T dO and dK += dS^T Q once the half's softmax is
+      // done (dQ^T first, so that its read-out overlaps dV and dK)
       auto issue_acc = [&](int u, int hh) -> bool {
         const int v = 2 * u + hh, slot = v % kRing;
         if (!mbar_wait(&bar->p_full[hh], u & 1, p.err, abort)) return false;
@@ -211,18 +215,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t aQ = smem_u32(sm + kOffRing + slot * 2 * kHalfTile);
         const uint32_t adO = aQ + kHalfTile;
         const uint32_t tS = tmem + hh * 128;
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          mma_ts(tmem + 256, tS + kk * 8, desc_mnmajor(adO, kk, kHalfBox), id_acc, first_acc ? 0u : 1u);
-          mma_ts(tmem + 384, tS + 32 + kk * 8, desc_mnmajor(aQ, kk, kHalfBox), id_acc, first_acc ? 0u : 1u);
-          first_acc = false;
-        }
-        mma_commit(&bar->hs_empty[slot]);
         const uint32_t adS = smem_u32(sm + kOffDS + hh * kHalfTile);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           mma_ss(tS + 64, desc_mnmajor(aK, kk), desc_mnmajor(adS, kk, kHalfBox), id_dq, kk > 0);
         mma_commit(&bar->dq_full[hh]);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          // query columns [16 kk, 16 kk + 16): packed P^T / dS^T of column group kk / 2
+          const uint32_t a = tS + 32 * (kk >> 1) + 8 * (kk & 1);
+          mma_ts(tmem + 256, a, desc_mnmajor(adO, kk, kHalfBox), id_acc, first_acc ? 0u : 1u);
+          mma_ts(tmem + 384, a + 16, desc_mnmajor(aQ, kk, kHalfBox), id_acc, first_acc ? 0u : 1u);
+          first_acc = false;
+        }
+        mma_commit(&bar->hs_empty[slot]);
         return true;
       };
       // half b's softmax overlaps the next step's S/dP of half a, and vice versa
@@ -236,9 +242,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(&bar->acc_full);
       mbar_wait(&bar->acc_full, 0, p.err, nullptr);
     }
-  } else if (warp < 6) {
+  } else if (warp < 10) {
     // ------------------------------------------------------------------ softmax
     const int j = (warp & 3) * 32 + lane;  // key row of the page
+    const int hc = (warp - 2) >> 2;        // query columns [32 hc, 32 hc + 32) of each half
     const uint32_t lane_off = tmem_lane_base(warp);
     bool ok = true;
     for (int u = 0; ok && u < n_steps; ++u) {
@@ -250,51 +257,43 @@ __global__ void __launch_bounds__(kThreads, 1)
              mbar_wait(&bar->hs_full[slot], (v / kRing) & 1, p.err, abort);
         if (!ok) break;
         tc_fence_after();
-        uint32_t sr[64], dr[64];
-        {
-          const uint32_t base = tmem + lane_off + hh * 128;
-          tmem_ld32(base + 0, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-          tmem_ld32(base + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-          tmem_ld32(base + 64, *reinterpret_cast<uint32_t(*)[32]>(&dr[0]));
-          tmem_ld32(base + 96, *reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
-          tmem_wait_ld();
+        const uint32_t base = tmem + lane_off + hh * 128 + 32 * hc;
+        uint32_t sr[32], dr[32];
+        tmem_ld32(base, sr);
+        tmem_ld32(base + 64, dr);
+        tmem_wait_ld();
+        const float4* vs4 = reinterpret_cast<const float4*>(vec + slot * 2 * kHalf) + 8 * hc;  // lse2, D
+        const int qbase = hh * kHalf + 32 * hc;  // query row (within the tile) of this thread's column 0
+        const bool masked = diag && (j > qbase);  // some column is in the key's future
+        uint32_t pk[16], dk[16];
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 L = vs4[c4], Dv = vs4[16 + c4];
+          const float l4[4] = {L.x, L.y, L.z, L.w}, d4[4] = {Dv.x, Dv.y, Dv.z, Dv.w};
+          float pr[4], dsr[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int i = 4 * c4 + e;
+            float pv = ex2_approx(fmaf(__uint_as_float(sr[i]), p.scale_log2, -l4[e]));
+            if (masked && j > qbase + i) pv = 0.f;
+            pr[e] = pv;
+            dsr[e] = pv * (__uint_as_float(dr[i]) - d4[e]);
+          }
+          pk[2 * c4] = pack_bf16x2(pr[0], pr[1]);
+          pk[2 * c4 + 1] = pack_bf16x2(pr[2], pr[3]);
+          dk[2 * c4] = pack_bf16x2(dsr[0], dsr[1]);
+          dk[2 * c4 + 1] = pack_bf16x2(dsr[2], dsr[3]);
         }
-        const float4* vs4 = reinterpret_cast<const float4*>(vec + slot * 2 * kHalf);  // lse2[64], D[64]
-        const int qbase = hh * kHalf;  // query row (within the tile) of column 0
-        const bool masked = diag && (j > qbase);  // some column of this half is in the key's future
-        const uint32_t base = tmem + lane_off + hh * 128;
+        // P^T and dS^T go over this thread's own (already loaded) S^T columns
+        tmem_st16(base, pk);
+        tmem_st16(base + 16, dk);
+        // dS^T row j, query columns [32 hc, 32 hc + 32): four 16-byte chunks of the swizzled tile
         uint8_t* drow = sm + kOffDS + hh * kHalfTile + j * 128;
 #pragma unroll
-        for (int part = 0; part < 2; ++part) {  // 32 query columns at a time
-          uint32_t pk[16], dk[16];
-#pragma unroll
-          for (int c4 = 0; c4 < 8; ++c4) {
-            const float4 L = vs4[part * 8 + c4], Dv = vs4[16 + part * 8 + c4];
-            const float l4[4] = {L.x, L.y, L.z, L.w}, d4[4] = {Dv.x, Dv.y, Dv.z, Dv.w};
-            float pr[4], dsr[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int i = part * 32 + 4 * c4 + e;
-              float pv = ex2_approx(fmaf(__uint_as_float(sr[i]), p.scale_log2, -l4[e]));
-              if (masked && j > qbase + i) pv = 0.f;
-              pr[e] = pv;
-              dsr[e] = pv * (__uint_as_float(dr[i]) - d4[e]);
-            }
-            pk[2 * c4] = pack_bf16x2(pr[0], pr[1]);
-            pk[2 * c4 + 1] = pack_bf16x2(pr[2], pr[3]);
-            dk[2 * c4] = pack_bf16x2(dsr[0], dsr[1]);
-            dk[2 * c4 + 1] = pack_bf16x2(dsr[2], dsr[3]);
-          }
-          // the whole half was already loaded into registers, so its TMEM columns may be overwritten
-          tmem_st16(base + part * 16, pk);
-          tmem_st16(base + 32 + part * 16, dk);
-          // dS^T row j, query columns [32 part, 32 part + 32): four 16-byte chunks of the swizzled tile
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int chunk = part * 4 + c;
-            uint4 w = make_uint4(dk[4 * c], dk[4 * c + 1], dk[4 * c + 2], dk[4 * c + 3]);
-            *reinterpret_cast<uint4*>(drow + ((chunk ^ (j & 7)) * 16)) = w;
-          }
+        for (int c = 0; c < 4; ++c) {
+          const int chunk = hc * 4 + c;
+          uint4 w = make_uint4(dk[4 * c], dk[4 * c + 1], dk[4 * c + 2], dk[4 * c + 3]);
+          *reinterpret_cast<uint4*>(drow + ((chunk ^ (j & 7)) * 16)) = w;
         }
         tmem_wait_st();
         fence_proxy_async_smem();
@@ -302,17 +301,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&bar->p_full[hh]);
       }
     }
-    // epilogue: this CTA's rows of the gradient pool += scale * dK, dV
+    // epilogue: this CTA's rows of the gradient pool += scale * dK, dV (64 columns per thread)
     if (ok && mbar_wait(&bar->acc_full, 0, p.err, abort)) {
       tc_fence_after();
-      const size_t row = (((size_t)phys * p.Hkv + h) * kTile + j) * kD;
+      const size_t row = (((size_t)phys * p.Hkv + h) * kTile + j) * kD + 64 * hc;
       float4* gdv = reinterpret_cast<float4*>(p.dv_pool + row);
       float4* gdk = reinterpret_cast<float4*>(p.dk_pool + row);
 #pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int cc = 0; cc < 2; ++cc) {
         uint32_t a[32], b[32];
-        tmem_ld32(tmem + lane_off + 256 + cc * 32, a);
-        tmem_ld32(tmem + lane_off + 384 + cc * 32, b);
+        tmem_ld32(tmem + lane_off + 256 + 64 * hc + cc * 32, a);
+        tmem_ld32(tmem + lane_off + 384 + 64 * hc + cc * 32, b);
         tmem_wait_ld();
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
@@ -335,23 +334,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------------ dQ read-out
     const int col = (warp & 3) * 32 + lane;  // head-dim column == TMEM lane of dQ^T
     const uint32_t lane_off = tmem_lane_base(warp);
-    const bool leader = (warp == 6 && lane == 0);
+    const bool leader = (warp == 10 && lane == 0);
     float* stage = reinterpret_cast<float*>(sm + kOffStage);
     bool ok = true;
     int piece = 0;
-    for (int u = 0; ok && u < n_steps; ++u) {
+    // On an abort every thread still runs all named barriers (only the work is skipped).
+    for (int u = 0; u < n_steps; ++u) {
       const int t = t0 + u / p.G, g = u % p.G;
       const int hq = h * p.G + g;
       for (int hh = 0; hh < 2; ++hh) {
-        ok = mbar_wait(&bar->dq_full[hh], u & 1, p.err, abort);
-        if (!ok) break;
-        tc_fence_after();
         uint32_t r[64];
-        tmem_ld32(tmem + lane_off + hh * 128 + 64, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-        tmem_ld32(tmem + lane_off + hh * 128 + 96, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(&bar->dq_free[hh]);
+        if (ok) ok = mbar_wait(&bar->dq_full[hh], u & 1, p.err, abort);
+        if (ok) {
+          tc_fence_after();
+          tmem_ld32(tmem + lane_off + hh * 128 + 64, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+          tmem_ld32(tmem + lane_off + hh * 128 + 96, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+          tmem_wait_ld();
+          tc_fence_before();
+          mbar_arrive(&bar->dq_free[hh]);
+        }
         const int q0 = t * kTile + hh * kHalf;
 #pragma unroll
         for (int pc = 0; pc < kHalf / kPieceRows; ++pc, ++piece) {
@@ -359,11 +360,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (leader) bulk_wait_read<1>();  // the reduce that last read this buffer is done
           named_bar_sync(1, 128);
           float* st = stage + buf * (kPieceRows * kD);
+          if (ok) {
 #pragma unroll
-          for (int rr = 0; rr < kPieceRows; ++rr) st[rr * kD + col] = __uint_as_float(r[pc * kPieceRows + rr]);
+            for (int rr = 0; rr < kPieceRows; ++rr) st[rr * kD + col] = __uint_as_float(r[pc * kPieceRows + rr]);
+          }
           fence_proxy_async_smem();
           named_bar_sync(1, 128);
-          if (leader) {
+          if (leader && ok) {
             const int r0 = q0 + pc * kPieceRows;
             const int nrows = min(kPieceRows, p.n_q - r0);
             if (nrows > 0) {
