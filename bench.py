@@ -128,7 +128,7 @@ class Step:
         self.o = torch.empty((C, w.n_q_heads, w.head_dim), dtype=w.torch_dtype, device=dev)
         self.lse = torch.empty((w.n_q_heads, C), dtype=torch.float32, device=dev)
         self.dq = [torch.empty_like(ch["q"]) for ch in self.chunks]
-        self.fwd_events, self.bwd_events = [], []
+        self.fwd_events, self.bwd_events, self.app_events, self.sel_events = [], [], [], []
         self.side = torch.cuda.Stream(device=dev) if self.offload else None
 
     def run(self, record=False):
@@ -138,8 +138,9 @@ class Step:
         L.oomb_pool_reset(h)
         for c, ch in enumerate(self.chunks):
             start, n = w.chunk_bounds(c)
-            L.oomb_kv_append(h, ch["k"], ch["v"], start)
-            L.oomb_page_select(h, ch["q"], start, w.top_k, w.n_sink, self.sel[c], self.cnt[c], self.ws_sel)
+            self._timed(record, self.app_events, c, L.oomb_kv_append, h, ch["k"], ch["v"], start)
+            self._timed(record, self.sel_events, c, L.oomb_page_select, h, ch["q"], start, w.top_k, w.n_sink,
+                        self.sel[c], self.cnt[c], self.ws_sel)
             self._fwd(c, ch, start, n, record)
         for c in range(w.n_chunks - 1, -1, -1):
             start, n = w.chunk_bounds(c)
@@ -201,6 +202,34 @@ class Step:
             self._bwd(c, self.chunks[c], start, n, record)
             used[c] = ev()
             used[c].record(main)
+
+    def _timed(self, record, events, c, fn, *args):
+        if not record:
+            return fn(*args)
+        e0, e1 = self.torch.cuda.Event(enable_timing=True), self.torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn(*args)
+        e1.record()
+        events.append((e0, e1, c))
+
+    def hbm_bytes(self):
+        """Algorithmic HBM bytes per call of append and select, per chunk."""
+        w = self.w
+        esz = 2 if w.dtype == "bf16" else 4
+        app, sel = {}, {}
+        for c in range(w.n_chunks):
+            start, n = w.chunk_bounds(c)
+            n_pages = -(-n // w.page)
+            # read K,V; write K,V; zero dK,dV rows (whole pages); summary rows
+            app[c] = (n * w.n_kv_heads * w.head_dim * esz * 2 * 2
+                      + n_pages * w.page * w.n_kv_heads * w.head_dim * 4 * 2
+                      + n_pages * w.n_kv_heads * w.head_dim * 4)
+            n_hist = start // w.page
+            cand = max(0, n_hist - w.n_sink)
+            scored = w.top_k >= 0 and cand > w.top_k
+            sel[c] = ((n * w.n_q_heads * w.head_dim * esz + cand * w.n_kv_heads * w.head_dim * 4
+                       + 2 * cand * w.n_kv_heads * 4) if scored else 0) + w.n_kv_heads * w.max_sel * 4
+        return app, sel
 
     def _bwd(self, c, ch, start, n, record):
         L, torch, w = self.L, self.torch, self.w
@@ -398,6 +427,14 @@ def main():
     bwd_tflops = sum(bwd_fl) / (sum(bwd_ms) * 1e-3) / 1e12
     fwd_tflops = sum(fwd_fl) / (sum(fwd_ms) * 1e-3) / 1e12
     peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+    app_b, sel_b = step.hbm_bytes()
+    def gbs(events, nbytes):
+        if not events:
+            return None
+        t = sum(a.elapsed_time(b) for a, b, _ in events) * 1e-3
+        return sum(nbytes[c] for _, _, c in events) / t / 1e9 if t > 0 else None
+    app_gbs, sel_gbs = gbs(step.app_events, app_b), gbs(step.sel_events, sel_b)
+    hbm_peak = peaks.get("hbm_gbs", 6783.0)
     value = credited / (ms * 1e-3) / 1e12 * world
     tokens_per_s = w.seq / (ms * 1e-3) * world
 
@@ -417,6 +454,12 @@ def main():
                          "peak": peak, "unit": "TFLOP/s", "frac": round(bwd_tflops / peak, 4),
                          "peak_source": peaks.get("source", "") + " (bf16 dense, sustained)",
                          "traffic": None},
+            "append_call": {"gbs": round(app_gbs, 1) if app_gbs else None,
+                            "frac_of_hbm": round(app_gbs / hbm_peak, 3) if app_gbs else None,
+                            "bytes_per_token_per_kv_head": 2 * 2 * w.head_dim * (2 if w.dtype == "bf16" else 4)
+                            + 2 * w.head_dim * 4},
+            "select_call": {"gbs": round(sel_gbs, 1) if sel_gbs else None,
+                            "frac_of_hbm": round(sel_gbs / hbm_peak, 3) if sel_gbs else None},
             "gpu_launches": int(launches),
             "clocks": clk.summary()}
 
