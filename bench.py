@@ -35,6 +35,15 @@ FALLBACK_PEAKS = {"hbm_gbs": 6783.0, "bf16_tflops": 1875.1, "bf16_tflops_sustain
                   "source": "driver-measured GB300 figures quoted in the repository's baseline notes"}
 
 
+_T0 = time.time()
+
+
+def log(msg: str) -> None:
+    """Progress line on stderr (the JSON result goes alone to stdout)."""
+    sys.stderr.write(f"[bench {time.time() - _T0:7.1f}s] {msg}\n")
+    sys.stderr.flush()
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -262,24 +271,43 @@ class Step:
 
     def pairs_per_chunk(self):
         """Selected, causally visible (query, key) pairs summed over query heads, per chunk."""
+        import numpy as np
         w = self.w
-        sel, cnt = self.sel.cpu(), self.cnt.cpu()
+        sel, cnt = self.sel.cpu().numpy(), self.cnt.cpu().numpy()
         out = []
         for c in range(w.n_chunks):
             start, n = w.chunk_bounds(c)
             first_own = start // w.page
             tot = 0
             for hk in range(w.n_kv_heads):
-                for p in sel[c, hk, : int(cnt[c, hk])].tolist():
-                    k0 = p * w.page
-                    k1 = min(k0 + w.page, start + n)
-                    if p < first_own:
-                        tot += (k1 - k0) * n
-                    else:  # own page: row i (absolute start+i) sees keys <= start+i
-                        for kpos in range(k0, k1):
-                            tot += start + n - kpos
+                pages = sel[c, hk, : int(cnt[c, hk])].astype(np.int64)
+                k0 = pages * w.page
+                m = np.minimum(k0 + w.page, start + n) - k0  # keys present in the page
+                hist = pages < first_own
+                tot += int((m[hist] * n).sum())
+                # own page: row at absolute position start+i sees keys <= start+i, i.e. the
+                # m keys from k0 contribute sum_{x<m} (start + n - k0 - x)
+                mo, ko = m[~hist], k0[~hist]
+                tot += int((mo * (start + n - ko) - mo * (mo - 1) // 2).sum())
             out.append(tot * w.group)
         return out
+
+
+def reduce_max_ms(ms: float, world: int, device) -> float:
+    """Step time of the whole job: the maximum over ranks (replicas run independently)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, ms_max: float, world: int) -> float:
+    """Whole-job throughput: every rank processes the same units (weak scaling) and the
+    job takes as long as its slowest rank."""
+    return units_per_rank * world / (ms_max * 1e-3)
 
 
 def oracle_sample_seconds(w, budget_s=20.0):
@@ -388,12 +416,17 @@ def main():
         if world > 1:
             dist.barrier()
 
+    log(f"workload {w.name}: building inputs and pool")
     step = Step(w, dev)
-    for _ in range(max(3, args.warmup)):
-        step.run()
     torch.cuda.synchronize()
+    log("warm-up")
+    for i in range(max(3, args.warmup)):
+        step.run()
+        torch.cuda.synchronize()
+        log(f"warm-up step {i} done")
     L.oomb_check(step.pool.handle)
     pairs = step.pairs_per_chunk()
+    log("credited pairs counted; timed steps")
     credited = sum(pairs) * 14 * w.head_dim
     fwd_flops = {c: p * 4 * w.head_dim for c, p in enumerate(pairs)}
     bwd_flops = {c: p * 10 * w.head_dim for c, p in enumerate(pairs)}
@@ -411,11 +444,7 @@ def main():
         torch.cuda.synchronize()
         barrier()
     launches = L.oomb_launch_count() - launches0
-    ms = e0.elapsed_time(e1) / args.steps
-    t = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms = float(t.item())
+    ms = reduce_max_ms(e0.elapsed_time(e1) / args.steps, world, dev)
     L.oomb_check(step.pool.handle)
 
     # per-kernel-call roofline: the backward (dominant) and forward calls
@@ -435,8 +464,8 @@ def main():
         return sum(nbytes[c] for _, _, c in events) / t / 1e9 if t > 0 else None
     app_gbs, sel_gbs = gbs(step.app_events, app_b), gbs(step.sel_events, sel_b)
     hbm_peak = peaks.get("hbm_gbs", 6783.0)
-    value = credited / (ms * 1e-3) / 1e12 * world
-    tokens_per_s = w.seq / (ms * 1e-3) * world
+    value = job_throughput(credited, ms, world) / 1e12
+    tokens_per_s = job_throughput(w.seq, ms, world)
 
     line = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": max(3, args.warmup), "ms_per_step": round(ms, 3), "higher_is_better": True,
