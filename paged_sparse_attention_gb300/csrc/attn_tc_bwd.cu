@@ -231,13 +231,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&bar->hs_empty[slot]);
         return true;
       };
-      // half b's softmax overlaps the next step's S/dP of half a, and vice versa
-      if (ok) ok = issue_sdp(0, 0) && issue_sdp(0, 1);
-      for (int u = 0; ok && u < n_steps; ++u) {
-        ok = issue_acc(u, 0);
-        if (ok && u + 1 < n_steps) ok = issue_sdp(u + 1, 0);
-        if (ok) ok = issue_acc(u, 1);
-        if (ok && u + 1 < n_steps) ok = issue_sdp(u + 1, 1);
+      // Each TMEM half region alternates S/dP(u) -> acc(u) -> S/dP(u+1); the two regions
+      // are independent, so whichever region's next group is ready is issued (the
+      // softmax of one half then overlaps the other half's MMAs).  Gives up after
+      // ~2^31 cycles without progress.
+      int next_sdp[2] = {0, 0}, next_acc[2] = {0, 0};
+      long long last = clock64();
+      while (ok && (next_acc[0] < n_steps || next_acc[1] < n_steps)) {
+        bool did = false;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int ua = next_acc[hh];
+          if (ua < next_sdp[hh] && mbar_try_wait(&bar->p_full[hh], ua & 1)) {
+            ok = issue_acc(ua, hh);
+            ++next_acc[hh];
+            did = true;
+          }
+          const int us = next_sdp[hh];
+          if (ok && us < n_steps && us == next_acc[hh]) {
+            const int v = 2 * us + hh;
+            if (mbar_try_wait(&bar->hs_full[v % kRing], (v / kRing) & 1) &&
+                (us == 0 || mbar_try_wait(&bar->dq_free[hh], (us - 1) & 1))) {
+              ok = issue_sdp(us, hh);
+              ++next_sdp[hh];
+              did = true;
+            }
+          }
+        }
+        if (did) {
+          last = clock64();
+        } else if (*abort) {
+          ok = false;
+        } else if (clock64() - last > (1ll << 31)) {
+          atomicOr(p.err, kErrMbarTimeout);
+          *abort = 1;
+          ok = false;
+        }
       }
       mma_commit(&bar->acc_full);
       mbar_wait(&bar->acc_full, 0, p.err, nullptr);
@@ -255,6 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int v = 2 * u + hh, slot = v % kRing;
         ok = mbar_wait(&bar->s_full[hh], u & 1, p.err, abort) &&
              mbar_wait(&bar->hs_full[slot], (v / kRing) & 1, p.err, abort);
+        ok = __all_sync(0xffffffffu, ok);  // TMEM loads and stores below are warp-collective
         if (!ok) break;
         tc_fence_after();
         const uint32_t base = tmem + lane_off + hh * 128 + 32 * hc;
@@ -302,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     // epilogue: this CTA's rows of the gradient pool += scale * dK, dV (64 columns per thread)
-    if (ok && mbar_wait(&bar->acc_full, 0, p.err, abort)) {
+    if (__all_sync(0xffffffffu, ok && mbar_wait(&bar->acc_full, 0, p.err, abort))) {
       tc_fence_after();
       const size_t row = (((size_t)phys * p.Hkv + h) * kTile + j) * kD + 64 * hc;
       float4* gdv = reinterpret_cast<float4*>(p.dv_pool + row);
@@ -345,6 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int hh = 0; hh < 2; ++hh) {
         uint32_t r[64];
         if (ok) ok = mbar_wait(&bar->dq_full[hh], u & 1, p.err, abort);
+        ok = __all_sync(0xffffffffu, ok);
         if (ok) {
           tc_fence_after();
           tmem_ld32(tmem + lane_off + hh * 128 + 64, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));

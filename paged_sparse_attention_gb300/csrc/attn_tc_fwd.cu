@@ -11,8 +11,9 @@
 // and pages after t (skipped).  CTAs are ordered heaviest tile first.
 //
 // Warp roles (320 threads):
-//   warp 0     TMA producer: Q once, then each selected page's K and V tile
-//              (3-stage ring), gathered through the page table.
+//   warp 0     TMA producer: Q once, then each selected page's K tile (4-stage
+//              ring, freed as soon as S has read it) and V tile (2-stage ring,
+//              freed after PV), gathered through the page table.
 //   warp 1     TMEM owner + MMA issuer: S_j = Q K_j^T into one of two TMEM S
 //              buffers -- S_{j+1} is computed while the softmax works on S_j --
 //              then O += P_j V_j with P_j (bf16, written over S_j) read from TMEM.
@@ -29,7 +30,8 @@ namespace {
 
 using namespace tc;
 
-constexpr int kStages = 3;
+constexpr int kKStages = 4;
+constexpr int kVStages = 2;
 constexpr int kThreads = 320;
 constexpr int kSoftmaxThreads = 256;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -49,9 +51,10 @@ struct FwdParams {
 
 struct __align__(8) FwdBarriers {
   uint64_t q_full;
-  uint64_t k_full[kStages];
-  uint64_t v_full[kStages];
-  uint64_t kv_empty[kStages];
+  uint64_t k_full[kKStages];
+  uint64_t k_empty[kKStages];
+  uint64_t v_full[kVStages];
+  uint64_t v_empty[kVStages];
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t o_done;
@@ -62,8 +65,8 @@ struct __align__(8) FwdBarriers {
 
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kTileBytes;
-constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;
-constexpr uint32_t kOffBar = kOffV + kStages * kTileBytes;
+constexpr uint32_t kOffV = kOffK + kKStages * kTileBytes;
+constexpr uint32_t kOffBar = kOffV + kVStages * kTileBytes;
 constexpr size_t kSmemBytes = 1024 + kOffBar + sizeof(FwdBarriers);
 
 // Leading selection entries (ascending pages) that are <= diag.  A negative entry
@@ -96,10 +99,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bar->q_full, 1);
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < kKStages; ++i) {
       mbar_init(&bar->k_full[i], 1);
+      mbar_init(&bar->k_empty[i], 1);
+    }
+    for (int i = 0; i < kVStages; ++i) {
       mbar_init(&bar->v_full[i], 1);
-      mbar_init(&bar->kv_empty[i], 1);
+      mbar_init(&bar->v_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar->s_full[i], 1);
@@ -136,36 +142,60 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx(&bar->q_full, kTileBytes);
       tma_load_3d(sm + kOffQ, &tq, &bar->q_full, 0, hq, t * kTile);
       tma_load_3d(sm + kOffQ + kHalfBytes, &tq, &bar->q_full, 64, hq, t * kTile);
-      int j = 0;
-      for (; j < n; ++j) {
-        const int st = j % kStages;
-        if (j >= kStages && !mbar_wait(&bar->kv_empty[st], ((j / kStages) - 1) & 1, p.err, abort)) break;
+      // K and V are issued independently, each as soon as its ring has a free slot
+      // (K runs up to kKStages pages ahead, V up to kVStages); the loop gives up after
+      // ~2^31 cycles without progress.
+      auto block_of = [&](int j) -> int64_t {
+        if (p.staged) return (int64_t)(p.stage_h0 + h) * p.stage_stride + j;
         const int pg = p.sel[(size_t)h * p.max_sel + j];
-        int64_t blk;
-        if (p.staged) {
-          blk = (int64_t)(p.stage_h0 + h) * p.stage_stride + j;
-        } else {
-          int phys = (pg < p.max_logical) ? p.table[pg] : -1;
-          if (phys < 0 || phys >= p.num_phys) {
-            atomicOr(p.err, OOMB_DEVERR_PAGE);
-            phys = 0;  // keep the pipeline consistent; the result is flagged as invalid
-          }
-          blk = (int64_t)phys * p.Hkv + h;
+        int phys = (pg >= 0 && pg < p.max_logical) ? p.table[pg] : -1;
+        if (phys < 0 || phys >= p.num_phys) {
+          atomicOr(p.err, OOMB_DEVERR_PAGE);
+          phys = 0;  // keep the pipeline consistent; the result is flagged as invalid
         }
-        const int row = (int)(blk * kTile);
-        mbar_arrive_expect_tx(&bar->k_full[st], kTileBytes);
-        tma_load_2d(sm + kOffK + st * kTileBytes, &tk, &bar->k_full[st], 0, row);
-        tma_load_2d(sm + kOffK + st * kTileBytes + kHalfBytes, &tk, &bar->k_full[st], 64, row);
-        mbar_arrive_expect_tx(&bar->v_full[st], kTileBytes);
-        tma_load_2d(sm + kOffV + st * kTileBytes, &tv, &bar->v_full[st], 0, row);
-        tma_load_2d(sm + kOffV + st * kTileBytes + kHalfBytes, &tv, &bar->v_full[st], 64, row);
+        return (int64_t)phys * p.Hkv + h;
+      };
+      int jk = 0, jv = 0;
+      long long last = clock64();
+      while (jk < n || jv < n) {
+        bool progressed = false;
+        if (jk < n) {
+          const int ks = jk % kKStages;
+          if (jk < kKStages || mbar_try_wait(&bar->k_empty[ks], ((jk / kKStages) - 1) & 1)) {
+            const int row = (int)(block_of(jk) * kTile);
+            mbar_arrive_expect_tx(&bar->k_full[ks], kTileBytes);
+            tma_load_2d(sm + kOffK + ks * kTileBytes, &tk, &bar->k_full[ks], 0, row);
+            tma_load_2d(sm + kOffK + ks * kTileBytes + kHalfBytes, &tk, &bar->k_full[ks], 64, row);
+            ++jk;
+            progressed = true;
+          }
+        }
+        if (jv < jk) {
+          const int vs = jv % kVStages;
+          if (jv < kVStages || mbar_try_wait(&bar->v_empty[vs], ((jv / kVStages) - 1) & 1)) {
+            const int row = (int)(block_of(jv) * kTile);
+            mbar_arrive_expect_tx(&bar->v_full[vs], kTileBytes);
+            tma_load_2d(sm + kOffV + vs * kTileBytes, &tv, &bar->v_full[vs], 0, row);
+            tma_load_2d(sm + kOffV + vs * kTileBytes + kHalfBytes, &tv, &bar->v_full[vs], 64, row);
+            ++jv;
+            progressed = true;
+          }
+        }
+        if (progressed) {
+          last = clock64();
+        } else if (*abort) {
+          break;
+        } else if (clock64() - last > (1ll << 31)) {
+          atomicOr(p.err, kErrMbarTimeout);
+          *abort = 1;
+          break;
+        }
       }
       // drain: every armed stage must have landed before the CTA may exit
-      for (int jj = (j > kStages ? j - kStages : 0); jj < j; ++jj) {
-        const int st = jj % kStages;
-        mbar_wait(&bar->k_full[st], (jj / kStages) & 1, p.err, nullptr);
-        mbar_wait(&bar->v_full[st], (jj / kStages) & 1, p.err, nullptr);
-      }
+      for (int jj = (jk > kKStages ? jk - kKStages : 0); jj < jk; ++jj)
+        mbar_wait(&bar->k_full[jj % kKStages], (jj / kKStages) & 1, p.err, nullptr);
+      for (int jj = (jv > kVStages ? jv - kVStages : 0); jj < jv; ++jj)
+        mbar_wait(&bar->v_full[jj % kVStages], (jj / kVStages) & 1, p.err, nullptr);
       mbar_wait(&bar->q_full, 0, p.err, nullptr);
     }
   } else if (warp == 1) {
@@ -176,27 +206,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t aQ = smem_u32(sm + kOffQ);
       const uint32_t tO = tmem + 256;
       auto issue_s = [&](int j) -> bool {
-        const int st = j % kStages;
-        if (!mbar_wait(&bar->k_full[st], (j / kStages) & 1, p.err, abort)) return false;
+        const int ks = j % kKStages;
+        if (!mbar_wait(&bar->k_full[ks], (j / kKStages) & 1, p.err, abort)) return false;
         tc_fence_after();
-        const uint32_t aK = smem_u32(sm + kOffK + st * kTileBytes);
+        const uint32_t aK = smem_u32(sm + kOffK + ks * kTileBytes);
         const uint32_t d = tmem + (j & 1) * 128;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) mma_ss(d, desc_kmajor(aQ, kk), desc_kmajor(aK, kk), idesc_s, kk > 0);
         mma_commit(&bar->s_full[j & 1]);
+        mma_commit(&bar->k_empty[ks]);
         return true;
       };
       auto issue_pv = [&](int j) -> bool {
-        const int st = j % kStages;
+        const int vs = j % kVStages;
         if (!mbar_wait(&bar->p_full[j & 1], (j >> 1) & 1, p.err, abort)) return false;
-        if (!mbar_wait(&bar->v_full[st], (j / kStages) & 1, p.err, abort)) return false;
+        if (!mbar_wait(&bar->v_full[vs], (j / kVStages) & 1, p.err, abort)) return false;
         tc_fence_after();
-        const uint32_t aV = smem_u32(sm + kOffV + st * kTileBytes);
+        const uint32_t aV = smem_u32(sm + kOffV + vs * kTileBytes);
         const uint32_t a = tmem + (j & 1) * 128;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           mma_ts(tO, a + kk * 8, desc_mnmajor(aV, kk), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bar->kv_empty[st]);
+        mma_commit(&bar->v_empty[vs]);
         mma_commit(&bar->o_done);
         return true;
       };
@@ -228,6 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t sr[64];
       float my_max = -INFINITY;
       if (ok) ok = mbar_wait(&bar->s_full[b], (j >> 1) & 1, p.err, abort);
+      ok = __all_sync(0xffffffffu, ok);  // TMEM loads and stores below are warp-collective
       if (ok) {
         tc_fence_after();
         tmem_ld32(tS + hc * 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
@@ -276,11 +308,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       l += (sum[0] + sum[1]) + (sum[2] + sum[3]);
       if (j > 0) {  // PV of the previous page is done: O may be rescaled
-        ok = mbar_wait(&bar->o_done, (j - 1) & 1, p.err, abort);
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar->o_done, (j - 1) & 1, p.err, abort));
         if (!ok) continue;
         tc_fence_after();
       }
-      if (rescale_o) {
+      // The rescale is decided per row but the TMEM accesses are warp-collective: the warp
+      // rescales when any of its rows needs it, the other rows scale by alpha = 1 (exact).
+      if (__any_sync(0xffffffffu, rescale_o)) {
+        if (!rescale_o) alpha = 1.f;
 #pragma unroll 1
         for (int cc = 0; cc < 2; ++cc) {
           uint32_t o[32];
@@ -301,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     named_bar_sync(bar_id, 64);
     const float l_row = l + bar->xchg[hc ^ 1][r];
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.o);
-    if (ok && n > 0 && mbar_wait(&bar->o_done, (n - 1) & 1, p.err, abort)) {
+    if (__all_sync(0xffffffffu, ok && n > 0 && mbar_wait(&bar->o_done, (n - 1) & 1, p.err, abort))) {
       tc_fence_after();
       const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
 #pragma unroll 1

@@ -205,3 +205,34 @@ def test_offload_matches_resident(name):
             assert np.array_equal(x, y)
     res.pool.close()
     off.pool.close()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_single_row_rescale(dtype):
+    """One query row meets a key whose score jumps far above its running maximum on
+    a later page, while the other rows of its warp see ordinary scores: the online
+    softmax must rescale O for that row alone (and the warp must not diverge)."""
+    w = synth.scaled(QWEN, f"rescale_{dtype}", seq=1024, chunk=512, top_k=-1, plants=0, dtype=dtype)
+    chunks, _ = make_chunks(w, plants=False)
+    q_tok, k_tok = 512 + 37, 200  # query in chunk 1 (tile 0), key on page 1 (second page visited)
+    for g in range(w.group):      # every query head of KV head 0 gets its own spike key
+        kt = k_tok + 3 * g
+        qv = chunks[1]["q"][q_tok - 512 + g, g].float()
+        # scaled score q.k / sqrt(d) = 14: ~16 in log2 units above the row's earlier maximum
+        chunks[0]["k"][kt, 0] = (14.0 * math.sqrt(w.head_dim) * qv / qv.dot(qv)).to(w.torch_dtype)
+    order = synth.page_order(w).tolist()
+    ref = oracle_sweep(w, chunks, order)
+    run = GpuSweep(w, chunks, order, sel_override=ref["sel"])
+    assert run.err_bits == 0
+    tol = TOL[w.dtype]
+    for c in range(w.n_chunks):
+        assert O.rel_l2(f64(run.O[c]), ref["O"][c]) < tol, ("O", c)
+        assert O.rel_l2(f64(run.LSE[c]), ref["LSE"][c]) < tol, ("LSE", c)
+        assert O.rel_l2(f64(run.dQ[c]), ref["dQ"][c]) < tol, ("dQ", c)
+    # the spiked rows: LSE within rounding of the spike's own score
+    for g in range(w.group):
+        r = q_tok - 512 + g
+        assert abs(float(run.LSE[1][g, r]) - ref["LSE"][1][g, r]) < 1e-2 * abs(ref["LSE"][1][g, r])
+    rdk, rdv = ref["pool"].logical_grads()
+    assert O.rel_l2(f64(run.dK), rdk) < tol
+    assert O.rel_l2(f64(run.dV), rdv) < tol
