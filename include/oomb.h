@@ -81,6 +81,14 @@ typedef enum { OOMB_OP_SELECT = 0, OOMB_OP_BWD = 1 } oomb_op;
 #define OOMB_DEVERR_SEL 0x4u      /* selection index out of range */
 #define OOMB_DEVERR_TMEM 0x8u     /* tensor-memory allocation failed */
 
+/* Length of the pool's control block (oomb_pool_desc.error_word), in uint32.
+ * Word 0 holds the error bits above; words 4..11 hold the grid-barrier state of
+ * oomb_page_select (counters that the kernel returns to zero, and flags that it
+ * compares with a per-call epoch).  Because that state is per pool, page
+ * selections on one pool must not run concurrently (issue them on one stream,
+ * or order them with events). */
+#define OOMB_CTRL_WORDS 16
+
 typedef struct {
   int n_q_heads;         /* Hq */
   int n_kv_heads;        /* Hkv; Hq % Hkv == 0 */
@@ -95,7 +103,8 @@ typedef struct {
   float* dv_pool;        /* same */
   float* summary;        /* [num_phys, Hkv, d] fp32 device */
   int32_t* page_table;   /* [max_logical_pages] device; written by the library */
-  uint32_t* error_word;  /* one device uint32, zero at creation */
+  uint32_t* error_word;  /* control block: OOMB_CTRL_WORDS device uint32, all zero
+                            at creation; 16-byte aligned */
   const int32_t* page_order; /* optional host [num_phys]: order in which physical
                                 pages are handed out (copied at creation); NULL = 0..n-1 */
   int offload;           /* 1: k_pool/v_pool live in pinned host memory and the
@@ -140,6 +149,10 @@ OOMB_API oomb_status oomb_kv_append(oomb_pool* pool, const void* k, const void* 
  * sel_count[h].  q: [n_q, Hq, d] device.  q_start must be a multiple of P and
  * the chunk's own K/V already appended.  Workspace: oomb_workspace_size(
  * OOMB_OP_SELECT, n_q) bytes of device memory, contents scratch.
+ * Launch: one cooperative kernel (one CTA per SM) whose phases meet at grid
+ * barriers kept in the pool's control block, so selections on one pool must be
+ * ordered (one stream, or events).  A barrier wait that runs out (~1 s) sets
+ * OOMB_DEVERR_TIMEOUT; oomb_check reports it and clears the control block.
  * Errors: ARG (incl. max_sel too small), ALIGN, WORKSPACE, CUDA. */
 OOMB_API oomb_status oomb_page_select(oomb_pool* pool, const void* q, int64_t q_start, int n_q, int top_k, int n_sink,
                              int32_t* sel, int32_t* sel_count, int max_sel, void* workspace, size_t ws_bytes,
@@ -155,7 +168,7 @@ OOMB_API oomb_status oomb_page_select(oomb_pool* pool, const void* q, int64_t q_
  * synchronize the device or fail under memory pressure) is forbidden, or a C host
  * with no allocator of its own.  The caller still passes q, sel and sel_count.
  *  - Limit: returns OOMB_ERR_WORKSPACE when oomb_workspace_size(pool,
- *    OOMB_OP_SELECT, n_q) exceeds 4 MiB (e.g. more than 262,144 logical pages at
+ *    OOMB_OP_SELECT, n_q) exceeds 4 MiB (e.g. more than 229,248 logical pages at
  *    4 KV heads x head_dim 128).
  *  - Set-up: the first call on a device looks up the array's device address with
  *    cudaGetSymbolAddress while that device is current; make that first call

@@ -16,6 +16,7 @@ LIB_PATH = os.path.join(PKG, "liboomb.so")
 HEADER = os.path.join(os.path.dirname(PKG), "include", "oomb.h")
 
 OOMB_BF16, OOMB_FP32 = 0, 1
+OOMB_CTRL_WORDS = 16  # uint32 words of a pool's control block (error bits + selection barrier state)
 OOMB_OP_SELECT, OOMB_OP_BWD = 0, 1
 STATUS = {0: "OK", 1: "ERR_ARG", 2: "ERR_OUT_OF_PAGES", 3: "ERR_ALIGN", 4: "ERR_DTYPE", 5: "ERR_KERNEL",
           6: "ERR_TIMEOUT", 7: "ERR_CUDA", 8: "ERR_UNSUPPORTED", 9: "ERR_WORKSPACE"}

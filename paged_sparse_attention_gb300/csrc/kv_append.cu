@@ -6,9 +6,11 @@
 // pages; the KV gradients live in pages that share the same table.  The page
 // summary is the representative vector of 2.D, fixed as the mean key per page.
 //
-// One thread block per (new page, KV head, K-or-V).  HBM traffic per token and KV
-// head: read K,V (2 d esize), write K,V (2 d esize), zero dK,dV (2 d 4 bytes);
-// plus one fp32 summary row per page and head.
+// One thread block per (new page, KV head): it loads the page's K and V rows with
+// several 16-byte loads in flight per thread, sums the K rows for the summary from
+// the same registers (K is read once), writes both pages and zeroes both gradient
+// pages.  HBM traffic per token and KV head: read K,V (2 d esize), write K,V
+// (2 d esize), zero dK,dV (2 d 4 bytes); plus one fp32 summary row per page and head.
 #include "oomb_internal.h"
 
 namespace oomb {
@@ -16,6 +18,7 @@ namespace {
 
 constexpr int kAppendThreads = 256;
 constexpr int kMaxNewPerLaunch = 1024;
+constexpr int kRowsInFlight = 8;  // K and V rows loaded per thread before any store
 
 struct NewPages {
   int32_t phys[kMaxNewPerLaunch];
@@ -34,7 +37,7 @@ __global__ void __launch_bounds__(kAppendThreads)
                      float* __restrict__ dv_pool, float* __restrict__ summary, int32_t* __restrict__ table,
                      const T* __restrict__ k, const T* __restrict__ v, int64_t first_token, int64_t end_token,
                      int first_new_logical, const __grid_constant__ NewPages np, int n_new, uint32_t* err) {
-  const int i = blockIdx.x, h = blockIdx.y, which = blockIdx.z;
+  const int i = blockIdx.x, h = blockIdx.y;
   const int P = g.P, d = g.d, Hkv = g.Hkv;
   const int phys = np.phys[i];
   if (phys < 0 || phys >= g.num_phys) {
@@ -42,50 +45,56 @@ __global__ void __launch_bounds__(kAppendThreads)
     return;
   }
   const int64_t logical = (int64_t)first_new_logical + i;
-  if (which == 0 && h == 0 && threadIdx.x == 0) table[logical] = phys;
+  if (h == 0 && threadIdx.x == 0) table[logical] = phys;
   const int64_t t0 = logical * P;
   const int m = (int)(end_token - t0 < P ? end_token - t0 : P);  // tokens present in this page
 
   constexpr int VEC = 16 / sizeof(T);
-  const int nvec = d / VEC;  // 16-byte vectors per row
-  const size_t blk = ((size_t)phys * Hkv + h) * (size_t)P * d;
-  const T* src = (which == 0 ? k : v);
-  T* dst = (which == 0 ? k_pool : v_pool) + blk;
-  float* gdst = (which == 0 ? dk_pool : dv_pool) + blk;
-
-  // copy K or V rows (zero the absent tail rows of a partial page)
-  for (int idx = threadIdx.x; idx < P * nvec; idx += kAppendThreads) {
-    const int r = idx / nvec, c = idx % nvec;
-    uint4 val = make_uint4(0, 0, 0, 0);
-    if (r < m) {
-      const int64_t tok = t0 + r - first_token;
-      val = *reinterpret_cast<const uint4*>(src + ((size_t)tok * Hkv + h) * d + (size_t)c * VEC);
-    }
-    *reinterpret_cast<uint4*>(dst + (size_t)r * d + (size_t)c * VEC) = val;
-  }
-  // zero the gradient page
-  const int nvec4 = d / 4;
-  for (int idx = threadIdx.x; idx < P * nvec4; idx += kAppendThreads)
-    reinterpret_cast<float4*>(gdst)[idx] = make_float4(0.f, 0.f, 0.f, 0.f);
-
-  if (which != 0) return;
-  // mean key over the m tokens present: fixed-order reduction, deterministic.
-  __shared__ float part[kAppendThreads * VEC];
-  const int n_rg = kAppendThreads / nvec;
+  const int nvec = d / VEC;                 // 16-byte vectors per row
+  const int n_rg = kAppendThreads / nvec;   // rows per pass of the block
   const int c = threadIdx.x % nvec, rg = threadIdx.x / nvec;
+  const size_t blk = ((size_t)phys * Hkv + h) * (size_t)P * d;
+  const int64_t tok0 = t0 - first_token;    // row 0 of the page in the chunk's K/V
   float acc[VEC];
 #pragma unroll
   for (int e = 0; e < VEC; ++e) acc[e] = 0.f;
   if (rg < n_rg) {
-    for (int r = rg; r < m; r += n_rg) {
-      const int64_t tok = t0 + r - first_token;
-      const T* row = src + ((size_t)tok * Hkv + h) * d + (size_t)c * VEC;
-      uint4 raw = *reinterpret_cast<const uint4*>(row);
-      const T* x = reinterpret_cast<const T*>(&raw);
+    for (int rb = rg; rb < P; rb += n_rg * kRowsInFlight) {
+      uint4 kr[kRowsInFlight], vr[kRowsInFlight];
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) acc[e] += to_f<T>(x[e]);
+      for (int u = 0; u < kRowsInFlight; ++u) {
+        const int r = rb + u * n_rg;
+        kr[u] = vr[u] = make_uint4(0, 0, 0, 0);  // absent tail rows of a partial page are zero
+        if (r < m) {
+          const size_t off = ((size_t)(tok0 + r) * Hkv + h) * d + (size_t)c * VEC;
+          kr[u] = __ldcs(reinterpret_cast<const uint4*>(k + off));
+          vr[u] = __ldcs(reinterpret_cast<const uint4*>(v + off));
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kRowsInFlight; ++u) {
+        const int r = rb + u * n_rg;
+        if (r < P) {
+          const size_t off = blk + (size_t)r * d + (size_t)c * VEC;
+          *reinterpret_cast<uint4*>(k_pool + off) = kr[u];
+          *reinterpret_cast<uint4*>(v_pool + off) = vr[u];
+          const T* x = reinterpret_cast<const T*>(&kr[u]);
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) acc[e] += to_f<T>(x[e]);  // rows in ascending order per thread
+        }
+      }
     }
   }
+  // zero both gradient pages (streaming stores: they are next read by a later backward)
+  const int nvec4 = P * d / 4;
+  float4* gk = reinterpret_cast<float4*>(dk_pool + blk);
+  float4* gv = reinterpret_cast<float4*>(dv_pool + blk);
+  for (int idx = threadIdx.x; idx < nvec4; idx += kAppendThreads) {
+    __stcs(gk + idx, make_float4(0.f, 0.f, 0.f, 0.f));
+    __stcs(gv + idx, make_float4(0.f, 0.f, 0.f, 0.f));
+  }
+  // mean key over the m tokens present: fixed-order reduction, deterministic
+  __shared__ float part[kAppendThreads * VEC];
 #pragma unroll
   for (int e = 0; e < VEC; ++e) part[threadIdx.x * VEC + e] = acc[e];
   __syncthreads();
@@ -108,7 +117,7 @@ cudaError_t launch_kv_append(const Geometry& g, void* k_pool, void* v_pool, floa
     const int cnt = n_new - base < kMaxNewPerLaunch ? n_new - base : kMaxNewPerLaunch;
     NewPages np;
     for (int i = 0; i < cnt; ++i) np.phys[i] = new_phys[base + i];
-    dim3 grid(cnt, g.Hkv, 2);
+    dim3 grid(cnt, g.Hkv);
     if (g.dtype == OOMB_FP32) {
       kv_append_kernel<float><<<grid, kAppendThreads, 0, st>>>(
           g, (float*)k_pool, (float*)v_pool, dk_pool, dv_pool, summary, table, (const float*)k, (const float*)v,

@@ -17,6 +17,7 @@ struct oomb_pool {
   int64_t n_tokens = 0;
   int stage_buf = 0;
   bool table_dirty = true;  // device page table still needs its -1 fill
+  uint32_t select_epoch = 0;  // per-call tag of the selection kernel's grid barriers
 };
 
 namespace {
@@ -127,7 +128,7 @@ oomb_status oomb_pool_create(const oomb_pool_desc* desc, oomb_pool** out) {
   if (d.num_phys_pages <= 0 || d.max_logical_pages <= 0) return OOMB_ERR_ARG;
   if (!d.k_pool || !d.v_pool || !d.dk_pool || !d.dv_pool || !d.summary || !d.page_table || !d.error_word)
     return OOMB_ERR_ARG;
-  const void* ptrs[] = {d.k_pool, d.v_pool, d.dk_pool, d.dv_pool, d.summary};
+  const void* ptrs[] = {d.k_pool, d.v_pool, d.dk_pool, d.dv_pool, d.summary, d.error_word};
   for (const void* p : ptrs)
     if (!aligned(p, 16)) return OOMB_ERR_ALIGN;
   if (d.offload) {
@@ -242,8 +243,10 @@ oomb_status oomb_page_select(oomb_pool* p, const void* q, int64_t q_start, int n
   size_t need = select_workspace_bytes(p->g, n_q);
   if (!ws || ws_bytes < need) return OOMB_ERR_WORKSPACE;
   if (!aligned(ws, 16)) return OOMB_ERR_ALIGN;
+  if (++p->select_epoch == 0) p->select_epoch = 1;  // 0 is the flags' initial value
   return cuda_status(launch_page_select(p->g, p->d.summary, p->d.page_table, q, q_start, n_q, top_k, n_sink, sel,
-                                        sel_count, max_sel, ws, p->d.error_word, (cudaStream_t)stream));
+                                        sel_count, max_sel, ws, p->d.error_word, p->d.error_word,
+                                        p->select_epoch, (cudaStream_t)stream));
 }
 
 static AttnArgs make_args(oomb_pool* p, const void* q, int64_t q_start, int n_q, const int32_t* sel,
@@ -327,7 +330,9 @@ oomb_status oomb_check(oomb_pool* p, void* stream, uint32_t* bits_out) {
   uint32_t bits = 0;
   cudaError_t e = cudaStreamSynchronize(st);
   if (e == cudaSuccess) e = cudaMemcpy(&bits, p->d.error_word, sizeof(bits), cudaMemcpyDeviceToHost);
-  if (e == cudaSuccess && bits) e = cudaMemset(p->d.error_word, 0, sizeof(uint32_t));
+  // after an error the whole control block is cleared: a selection that gave up
+  // at a grid barrier may have left a counter behind
+  if (e == cudaSuccess && bits) e = cudaMemset(p->d.error_word, 0, OOMB_CTRL_WORDS * sizeof(uint32_t));
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (bits_out) *bits_out = bits;
   if (e != cudaSuccess) return cuda_status(e);

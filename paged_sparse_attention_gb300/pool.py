@@ -38,7 +38,7 @@ class PagedKVPool:
         self.dv_pool = torch.zeros(shape, dtype=torch.float32, device=self.device)
         self.summary = torch.zeros((num_phys_pages, n_kv_heads, head_dim), dtype=torch.float32, device=self.device)
         self.page_table = torch.empty(max_logical_pages, dtype=torch.int32, device=self.device)
-        self.error_word = torch.zeros(1, dtype=torch.int32, device=self.device)
+        self.error_word = torch.zeros(_lib.OOMB_CTRL_WORDS, dtype=torch.int32, device=self.device)
         self._order = None if page_order is None else page_order.to(torch.int32).contiguous().cpu()
         d = _lib.PoolDesc()
         d.n_q_heads, d.n_kv_heads, d.head_dim, d.page_size = n_q_heads, n_kv_heads, head_dim, page_size
