@@ -293,6 +293,33 @@ class Step:
         return out
 
 
+def same_size_gbs(nbytes: int, dev, kind: str) -> float:
+    """Bandwidth of a plain PyTorch kernel moving the same bytes from cold L2: a sum
+    over nbytes (kind "read") or a copy of nbytes / 2 (kind "copy", nbytes moved in
+    total).  Small transfers do not reach the large-copy peak; this is the
+    size-matched reference for the append and selection calls."""
+    import torch
+    n = max(16, int(nbytes if kind == "read" else nbytes // 2)) // 4
+    src = torch.ones(n, dtype=torch.float32, device=dev)
+    dst = torch.empty_like(src) if kind == "copy" else None
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    times = []
+    for i in range(7):
+        flush.fill_(i)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        if kind == "read":
+            src.sum()
+        else:
+            dst.copy_(src)
+        e1.record()
+        torch.cuda.synchronize()
+        if i:
+            times.append(e0.elapsed_time(e1))
+    times.sort()
+    return (n * 4 * (1 if kind == "read" else 2)) / (times[len(times) // 2] * 1e-3) / 1e9
+
+
 def reduce_max_ms(ms: float, world: int, device) -> float:
     """Step time of the whole job: the maximum over ranks (replicas run independently)."""
     if world <= 1:
@@ -463,6 +490,9 @@ def main():
         t = sum(a.elapsed_time(b) for a, b, _ in events) * 1e-3
         return sum(nbytes[c] for _, _, c in events) / t / 1e9 if t > 0 else None
     app_gbs, sel_gbs = gbs(step.app_events, app_b), gbs(step.sel_events, sel_b)
+    # size-matched references (largest call of each kind)
+    app_ref = same_size_gbs(max(app_b.values()), dev, "copy") if app_gbs else None
+    sel_ref = same_size_gbs(max(sel_b.values()), dev, "read") if sel_gbs else None
     hbm_peak = peaks.get("hbm_gbs", 6783.0)
     value = job_throughput(credited, ms, world) / 1e12
     tokens_per_s = job_throughput(w.seq, ms, world)
@@ -485,10 +515,14 @@ def main():
                          "traffic": None},
             "append_call": {"gbs": round(app_gbs, 1) if app_gbs else None,
                             "frac_of_hbm": round(app_gbs / hbm_peak, 3) if app_gbs else None,
+                            "same_size_copy_gbs": round(app_ref, 1) if app_ref else None,
+                            "frac_of_same_size_copy": round(app_gbs / app_ref, 3) if app_ref else None,
                             "bytes_per_token_per_kv_head": 2 * 2 * w.head_dim * (2 if w.dtype == "bf16" else 4)
                             + 2 * w.head_dim * 4},
             "select_call": {"gbs": round(sel_gbs, 1) if sel_gbs else None,
-                            "frac_of_hbm": round(sel_gbs / hbm_peak, 3) if sel_gbs else None},
+                            "frac_of_hbm": round(sel_gbs / hbm_peak, 3) if sel_gbs else None,
+                            "same_size_read_gbs": round(sel_ref, 1) if sel_ref else None,
+                            "frac_of_same_size_read": round(sel_gbs / sel_ref, 3) if sel_ref else None},
             "gpu_launches": int(launches),
             "clocks": clk.summary()}
 

@@ -82,11 +82,10 @@ typedef enum { OOMB_OP_SELECT = 0, OOMB_OP_BWD = 1 } oomb_op;
 #define OOMB_DEVERR_TMEM 0x8u     /* tensor-memory allocation failed */
 
 /* Length of the pool's control block (oomb_pool_desc.error_word), in uint32.
- * Word 0 holds the error bits above; words 4..11 hold the grid-barrier state of
- * oomb_page_select (counters that the kernel returns to zero, and flags that it
- * compares with a per-call epoch).  Because that state is per pool, page
- * selections on one pool must not run concurrently (issue them on one stream,
- * or order them with events). */
+ * Word 0 holds the error bits above; words 4..6 are the grid-barrier counters of
+ * oomb_page_select, which only grow (the library keeps their expected values on
+ * the host).  Because that state is per pool, page selections on one pool must
+ * not run concurrently (issue them on one stream, or order them with events). */
 #define OOMB_CTRL_WORDS 16
 
 typedef struct {
@@ -168,7 +167,7 @@ OOMB_API oomb_status oomb_page_select(oomb_pool* pool, const void* q, int64_t q_
  * synchronize the device or fail under memory pressure) is forbidden, or a C host
  * with no allocator of its own.  The caller still passes q, sel and sel_count.
  *  - Limit: returns OOMB_ERR_WORKSPACE when oomb_workspace_size(pool,
- *    OOMB_OP_SELECT, n_q) exceeds 4 MiB (e.g. more than 229,248 logical pages at
+ *    OOMB_OP_SELECT, n_q) exceeds 4 MiB (e.g. more than 225,280 logical pages at
  *    4 KV heads x head_dim 128).
  *  - Set-up: the first call on a device looks up the array's device address with
  *    cudaGetSymbolAddress while that device is current; make that first call

@@ -17,7 +17,7 @@ struct oomb_pool {
   int64_t n_tokens = 0;
   int stage_buf = 0;
   bool table_dirty = true;  // device page table still needs its -1 fill
-  uint32_t select_epoch = 0;  // per-call tag of the selection kernel's grid barriers
+  uint32_t bar_ctr[3] = {0, 0, 0};  // values of the selection kernel's barrier counters
 };
 
 namespace {
@@ -243,10 +243,9 @@ oomb_status oomb_page_select(oomb_pool* p, const void* q, int64_t q_start, int n
   size_t need = select_workspace_bytes(p->g, n_q);
   if (!ws || ws_bytes < need) return OOMB_ERR_WORKSPACE;
   if (!aligned(ws, 16)) return OOMB_ERR_ALIGN;
-  if (++p->select_epoch == 0) p->select_epoch = 1;  // 0 is the flags' initial value
   return cuda_status(launch_page_select(p->g, p->d.summary, p->d.page_table, q, q_start, n_q, top_k, n_sink, sel,
-                                        sel_count, max_sel, ws, p->d.error_word, p->d.error_word,
-                                        p->select_epoch, (cudaStream_t)stream));
+                                        sel_count, max_sel, ws, p->d.error_word, p->d.error_word, p->bar_ctr,
+                                        (cudaStream_t)stream));
 }
 
 static AttnArgs make_args(oomb_pool* p, const void* q, int64_t q_start, int n_q, const int32_t* sel,
@@ -332,7 +331,10 @@ oomb_status oomb_check(oomb_pool* p, void* stream, uint32_t* bits_out) {
   if (e == cudaSuccess) e = cudaMemcpy(&bits, p->d.error_word, sizeof(bits), cudaMemcpyDeviceToHost);
   // after an error the whole control block is cleared: a selection that gave up
   // at a grid barrier may have left a counter behind
-  if (e == cudaSuccess && bits) e = cudaMemset(p->d.error_word, 0, OOMB_CTRL_WORDS * sizeof(uint32_t));
+  if (e == cudaSuccess && bits) {
+    e = cudaMemset(p->d.error_word, 0, OOMB_CTRL_WORDS * sizeof(uint32_t));
+    for (uint32_t& c : p->bar_ctr) c = 0;
+  }
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (bits_out) *bits_out = bits;
   if (e != cudaSuccess) return cuda_status(e);

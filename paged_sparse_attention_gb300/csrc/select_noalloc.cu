@@ -18,8 +18,8 @@
 namespace {
 
 // Largest scratch the static array provides: 4 MiB.  It covers, for example,
-// 4 KV heads x head_dim 128 with up to 229,248 logical pages (29M tokens at 128
-// tokens per page), or 8 KV heads x head_dim 128 with up to 98,176.
+// 4 KV heads x head_dim 128 with up to 225,280 logical pages (28.8M tokens at 128
+// tokens per page), or 8 KV heads x head_dim 128 with up to 94,208.
 constexpr size_t kNoAllocSelectBytes = size_t(4) << 20;
 
 static __device__ __align__(256) unsigned char g_select_scratch[kNoAllocSelectBytes];

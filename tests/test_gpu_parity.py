@@ -236,3 +236,48 @@ def test_single_row_rescale(dtype):
     rdk, rdv = ref["pool"].logical_grads()
     assert O.rel_l2(f64(run.dK), rdk) < tol
     assert O.rel_l2(f64(run.dV), rdv) < tol
+
+
+@pytest.mark.parametrize("pattern", ["all_equal", "alternating"])
+def test_select_exact_ties(pattern):
+    """Exactly tied page scores go to the lowest logical pages.  'all_equal' gives
+    every candidate the same summary (more tied keys than the threshold bin's
+    gather list holds); 'alternating' ties half of the candidates at the top."""
+    w = synth.scaled(QWEN, f"ties_{pattern}", seq=16 * 4224, chunk=16 * 2112, page=16, top_k=100, plants=0)
+    dev = torch.device("cuda")
+    order = synth.page_order(w)
+    pool = PagedKVPool(w.n_q_heads, w.n_kv_heads, w.head_dim, w.page, w.num_phys, w.n_pages, w.torch_dtype,
+                       dev, page_order=order)
+    opool = O.OraclePool(w.n_kv_heads, w.head_dim, w.page, w.num_phys, w.n_pages)
+    ws = pool.workspace(L.OOMB_OP_SELECT, w.chunk)
+    g = torch.Generator().manual_seed(7)
+    a = torch.randn(w.n_kv_heads, w.head_dim, generator=g)
+    b = torch.randn(w.n_kv_heads, w.head_dim, generator=g)
+    used = 0
+    for c in range(w.n_chunks):
+        start, n = w.chunk_bounds(c)
+        tok = torch.arange(start, start + n)
+        if pattern == "all_equal":
+            k = a.expand(n, -1, -1)
+        else:
+            k = torch.where(((tok // w.page) % 2 == 0)[:, None, None], a, b)
+        k = k.to(w.torch_dtype).contiguous()
+        v = torch.randn(n, w.n_kv_heads, w.head_dim, generator=g).to(w.torch_dtype)
+        L.oomb_kv_append(pool.handle, k.to(dev), v.to(dev), start)
+        npg = -(-n // w.page)
+        opool.append(k.double().numpy(), v.double().numpy(), start, order[used:used + npg].tolist())
+        used += npg
+    c = w.n_chunks - 1
+    start, n = w.chunk_bounds(c)
+    q = torch.randn(n, w.n_q_heads, w.head_dim, generator=g).to(w.torch_dtype)
+    sel = torch.full((w.n_kv_heads, w.max_sel), -1, dtype=torch.int32, device=dev)
+    cnt = torch.zeros(w.n_kv_heads, dtype=torch.int32, device=dev)
+    L.oomb_page_select(pool.handle, q.to(dev), start, w.top_k, w.n_sink, sel, cnt, ws)
+    ref = O.select_pages(opool, q.double().numpy(), start, w.top_k, w.n_sink)
+    n_cand = start // w.page - w.n_sink
+    assert n_cand > 2048
+    for h in range(w.n_kv_heads):
+        got = sel[h, : int(cnt[h])].cpu().numpy()
+        assert np.array_equal(got, np.asarray(ref[h])), (h, got[:8], ref[h][:8])
+    assert L.oomb_check(pool.handle) == 0
+    pool.close()
