@@ -231,42 +231,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&bar->hs_empty[slot]);
         return true;
       };
-      // Each TMEM half region alternates S/dP(u) -> acc(u) -> S/dP(u+1); the two regions
-      // are independent, so whichever region's next group is ready is issued (the
-      // softmax of one half then overlaps the other half's MMAs).  Gives up after
-      // ~2^31 cycles without progress.
-      int next_sdp[2] = {0, 0}, next_acc[2] = {0, 0};
-      long long last = clock64();
-      while (ok && (next_acc[0] < n_steps || next_acc[1] < n_steps)) {
-        bool did = false;
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int ua = next_acc[hh];
-          if (ua < next_sdp[hh] && mbar_try_wait(&bar->p_full[hh], ua & 1)) {
-            ok = issue_acc(ua, hh);
-            ++next_acc[hh];
-            did = true;
-          }
-          const int us = next_sdp[hh];
-          if (ok && us < n_steps && us == next_acc[hh]) {
-            const int v = 2 * us + hh;
-            if (mbar_try_wait(&bar->hs_full[v % kRing], (v / kRing) & 1) &&
-                (us == 0 || mbar_try_wait(&bar->dq_free[hh], (us - 1) & 1))) {
-              ok = issue_sdp(us, hh);
-              ++next_sdp[hh];
-              did = true;
-            }
-          }
-        }
-        if (did) {
-          last = clock64();
-        } else if (*abort) {
-          ok = false;
-        } else if (clock64() - last > (1ll << 31)) {
-          atomicOr(p.err, kErrMbarTimeout);
-          *abort = 1;
-          ok = false;
-        }
+      // half b's softmax overlaps the next step's S/dP of half a, and vice versa
+      if (ok) ok = issue_sdp(0, 0) && issue_sdp(0, 1);
+      for (int u = 0; ok && u < n_steps; ++u) {
+        ok = issue_acc(u, 0);
+        if (ok && u + 1 < n_steps) ok = issue_sdp(u + 1, 0);
+        if (ok) ok = issue_acc(u, 1);
+        if (ok && u + 1 < n_steps) ok = issue_sdp(u + 1, 1);
       }
       mma_commit(&bar->acc_full);
       mbar_wait(&bar->acc_full, 0, p.err, nullptr);

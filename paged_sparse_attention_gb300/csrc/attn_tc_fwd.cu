@@ -5,24 +5,27 @@
 // selected for its KV head hq/G that precede it causally; O and the natural-log
 // LSE are written.
 //
-// One CTA per (query head, 128-row query tile t).  The tile's rows are exactly the
-// tokens of the chunk's own page t, so its selected pages split into full pages
-// (history and own pages before t), the diagonal page t (causal mask key <= row)
-// and pages after t (skipped).  CTAs are ordered heaviest tile first.
+// One CTA per (query head, pair of 128-row query tiles A = 2u, B = 2u + 1).  A
+// tile's rows are exactly the tokens of the chunk's own page t, so its selected
+// pages are a prefix of the ascending selection: every entry <= t's page, the last
+// one being the diagonal page (causal mask key <= row).  Tile B's pages are A's
+// plus B's own diagonal page.  Both tiles share every K and V tile loaded.  CTAs
+// are ordered heaviest pair first.
 //
 // Warp roles (320 threads):
-//   warp 0     TMA producer: Q once, then each selected page's K tile (4-stage
-//              ring, freed as soon as S has read it) and V tile (2-stage ring,
-//              freed after PV), gathered through the page table.
-//   warp 1     TMEM owner + MMA issuer: S_j = Q K_j^T into one of two TMEM S
-//              buffers -- S_{j+1} is computed while the softmax works on S_j --
-//              then O += P_j V_j with P_j (bf16, written over S_j) read from TMEM.
-//   warps 2-9  softmax: two warps per TMEM lane quarter, each owning 64 of the 128
-//              key columns of its 32 query rows; the pair exchanges its partial row
-//              max through shared memory.  Base-2 online softmax with lazy
-//              rescaling of O (only when the row max grows by more than 2^8); each
-//              thread rescales and finally normalises its 64 columns of O.
-// TMEM columns: S0 [0,128), S1 [128,256), O [256,384).
+//   warp 0     TMA producer: both Q tiles once, then each selected page's K tile
+//              (3-stage ring, freed once both S tiles have read it) and V tile
+//              (2-stage ring, freed after both PV), gathered through the page table.
+//   warp 1     TMEM owner + MMA issuer.  Per page j the tensor core runs
+//              PV_A(j-1), S_A(j), PV_B(j-1), S_B(j): while the softmax of one tile
+//              works, the tensor core computes the other tile's products, so each
+//              softmax has the time of two MMAs before its PV is due.
+//              S = Q K^T into the tile's S columns; O += P V with P (bf16, written
+//              over S by the softmax) read from TMEM.
+//   warps 2-5  softmax of tile A, warps 6-9 softmax of tile B: one thread per query
+//              row holding all 128 key columns.  Base-2 online softmax with lazy
+//              rescaling of O (only when the row max grows by more than 2^8).
+// TMEM columns: S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
 #include "tc_common.cuh"
 
 namespace oomb {
@@ -30,10 +33,10 @@ namespace {
 
 using namespace tc;
 
-constexpr int kKStages = 4;
+constexpr int kKStages = 3;
 constexpr int kVStages = 2;
 constexpr int kThreads = 320;
-constexpr int kSoftmaxThreads = 256;
+constexpr int kGroupThreads = 128;         // softmax threads of one tile
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 struct FwdParams {
@@ -43,7 +46,7 @@ struct FwdParams {
   void* o;
   float* lse;
   uint32_t* err;
-  int max_sel, n_q, Hq, G, Hkv, num_phys, max_logical, n_tiles;
+  int max_sel, n_q, Hq, G, Hkv, num_phys, max_logical, n_tiles, n_pairs;
   int64_t q_start;
   float scale_log2;
   int staged, stage_h0, stage_stride;
@@ -55,19 +58,20 @@ struct __align__(8) FwdBarriers {
   uint64_t k_empty[kKStages];
   uint64_t v_full[kVStages];
   uint64_t v_empty[kVStages];
-  uint64_t s_full[2];
-  uint64_t p_full[2];
-  uint64_t o_done;
+  uint64_t s_full[2];  // per tile: S_j in TMEM
+  uint64_t p_full[2];  // per tile: P_j written over S_j (and O rescaled)
+  uint64_t o_done[2];  // per tile: PV_j finished
+  uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
-  float xchg[2][128];  // [column half][row]: partial row maxima, then (epilogue) partial row sums
 };
 
-constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = kTileBytes;
+constexpr uint32_t kOffQ = 0;                              // tiles A and B
+constexpr uint32_t kOffK = 2 * kTileBytes;
 constexpr uint32_t kOffV = kOffK + kKStages * kTileBytes;
 constexpr uint32_t kOffBar = kOffV + kVStages * kTileBytes;
 constexpr size_t kSmemBytes = 1024 + kOffBar + sizeof(FwdBarriers);
+static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 // Leading selection entries (ascending pages) that are <= diag.  A negative entry
 // is invalid (flagged by the producer) and ends the list.
@@ -90,11 +94,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int hq = blockIdx.x;
-  const int t = p.n_tiles - 1 - (int)blockIdx.y;  // heaviest tiles first
+  const int pair = p.n_pairs - 1 - (int)blockIdx.y;  // heaviest pairs first
+  const int tA = 2 * pair, tB = 2 * pair + 1;
+  const bool hasB = tB < p.n_tiles;
   const int h = hq / p.G;
-  const int diag = (int)(p.q_start / kTile) + t;
+  const int diagA = (int)(p.q_start / kTile) + tA;
   const int count = p.sel_count[h];
-  const int n = pages_upto(p, h, count, diag);  // pages this tile attends to
+  const int nA = pages_upto(p, h, count, diagA);
+  const int nB = hasB ? pages_upto(p, h, count, diagA + 1) : 0;
+  const int n = max(nA, nB);  // pages loaded
   volatile int* abort = &bar->abort;
 
   if (threadIdx.x == 0) {
@@ -109,9 +117,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar->s_full[i], 1);
-      mbar_init(&bar->p_full[i], kSoftmaxThreads);
+      mbar_init(&bar->p_full[i], kGroupThreads);
+      mbar_init(&bar->o_done[i], 1);
     }
-    mbar_init(&bar->o_done, 1);
+    mbar_init(&bar->mma_done, 1);
     bar->abort = 0;
     fence_mbar_init();
   }
@@ -139,12 +148,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
       }
-      mbar_arrive_expect_tx(&bar->q_full, kTileBytes);
-      tma_load_3d(sm + kOffQ, &tq, &bar->q_full, 0, hq, t * kTile);
-      tma_load_3d(sm + kOffQ + kHalfBytes, &tq, &bar->q_full, 64, hq, t * kTile);
-      // K and V are issued independently, each as soon as its ring has a free slot
-      // (K runs up to kKStages pages ahead, V up to kVStages); the loop gives up after
-      // ~2^31 cycles without progress.
+      mbar_arrive_expect_tx(&bar->q_full, (hasB ? 2u : 1u) * kTileBytes);
+      tma_load_3d(sm + kOffQ, &tq, &bar->q_full, 0, hq, tA * kTile);
+      tma_load_3d(sm + kOffQ + kHalfBytes, &tq, &bar->q_full, 64, hq, tA * kTile);
+      if (hasB) {
+        tma_load_3d(sm + kOffQ + kTileBytes, &tq, &bar->q_full, 0, hq, tB * kTile);
+        tma_load_3d(sm + kOffQ + kTileBytes + kHalfBytes, &tq, &bar->q_full, 64, hq, tB * kTile);
+      }
+      // K and V are issued independently, each as soon as its ring has a free slot;
+      // the loop gives up after ~2^31 cycles without progress.
       auto block_of = [&](int j) -> int64_t {
         if (p.staged) return (int64_t)(p.stage_h0 + h) * p.stage_stride + j;
         const int pg = p.sel[(size_t)h * p.max_sel + j];
@@ -203,90 +215,104 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && n > 0) {
       const uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
       const uint32_t idesc_o = idesc_bf16_f32(128, 128, false, true);
-      const uint32_t aQ = smem_u32(sm + kOffQ);
-      const uint32_t tO = tmem + 256;
-      auto issue_s = [&](int j) -> bool {
-        const int ks = j % kKStages;
-        if (!mbar_wait(&bar->k_full[ks], (j / kKStages) & 1, p.err, abort)) return false;
-        tc_fence_after();
-        const uint32_t aK = smem_u32(sm + kOffK + ks * kTileBytes);
-        const uint32_t d = tmem + (j & 1) * 128;
+      const int nt[2] = {nA, nB};
+      bool ok = mbar_wait(&bar->q_full, 0, p.err, abort);
+      // S_X(j) = Q_X K_j^T into the S columns of tile X (the K tile has landed)
+      auto issue_s = [&](int x, int j) {
+        const uint32_t aQ = smem_u32(sm + kOffQ + x * kTileBytes);
+        const uint32_t aK = smem_u32(sm + kOffK + (j % kKStages) * kTileBytes);
+        const uint32_t d = tmem + x * 128;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) mma_ss(d, desc_kmajor(aQ, kk), desc_kmajor(aK, kk), idesc_s, kk > 0);
-        mma_commit(&bar->s_full[j & 1]);
-        mma_commit(&bar->k_empty[ks]);
-        return true;
+        mma_commit(&bar->s_full[x]);
       };
-      auto issue_pv = [&](int j) -> bool {
-        const int vs = j % kVStages;
-        if (!mbar_wait(&bar->p_full[j & 1], (j >> 1) & 1, p.err, abort)) return false;
-        if (!mbar_wait(&bar->v_full[vs], (j / kVStages) & 1, p.err, abort)) return false;
+      // O_X += P_X(j) V_j once the softmax has written P_X(j) (the V tile has landed)
+      auto issue_pv = [&](int x, int j) -> bool {
+        if (!mbar_wait(&bar->p_full[x], j & 1, p.err, abort)) return false;
         tc_fence_after();
-        const uint32_t aV = smem_u32(sm + kOffV + vs * kTileBytes);
-        const uint32_t a = tmem + (j & 1) * 128;
+        const uint32_t aV = smem_u32(sm + kOffV + (j % kVStages) * kTileBytes);
+        const uint32_t a = tmem + x * 128, o = tmem + 256 + x * 128;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tO, a + kk * 8, desc_mnmajor(aV, kk), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bar->v_empty[vs]);
-        mma_commit(&bar->o_done);
+        for (int kk = 0; kk < 8; ++kk) mma_ts(o, a + kk * 8, desc_mnmajor(aV, kk), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bar->o_done[x]);
         return true;
       };
-      bool ok = mbar_wait(&bar->q_full, 0, p.err, abort) && issue_s(0);
+      // page 0: both S
+      if (ok) ok = mbar_wait(&bar->k_full[0], 0, p.err, abort);
+      if (ok) {
+        tc_fence_after();
+        for (int x = 0; x < 2; ++x)
+          if (0 < nt[x]) issue_s(x, 0);
+        mma_commit(&bar->k_empty[0]);
+      }
       for (int j = 0; ok && j < n; ++j) {
-        if (j + 1 < n) ok = issue_s(j + 1);  // S_{j+1} while the softmax works on S_j
-        if (ok) ok = issue_pv(j);
+        const int j1 = j + 1;
+        bool v_waited = false, k_waited = false;
+        for (int x = 0; ok && x < 2; ++x) {
+          if (j < nt[x]) {  // PV_X(j)
+            if (!v_waited) {
+              ok = mbar_wait(&bar->v_full[j % kVStages], (j / kVStages) & 1, p.err, abort);
+              v_waited = true;
+            }
+            ok = ok && issue_pv(x, j);
+            if (ok && (x == 1 || j >= nt[1])) mma_commit(&bar->v_empty[j % kVStages]);  // last PV of page j
+          }
+          if (ok && j1 < nt[x]) {  // S_X(j+1)
+            if (!k_waited) {
+              ok = mbar_wait(&bar->k_full[j1 % kKStages], (j1 / kKStages) & 1, p.err, abort);
+              k_waited = true;
+              if (ok) tc_fence_after();
+            }
+            if (ok) {
+              issue_s(x, j1);
+              if (x == 1 || j1 >= nt[1]) mma_commit(&bar->k_empty[j1 % kKStages]);  // last S of page j+1
+            }
+          }
+        }
       }
       // every issued MMA must finish before TMEM is released
-      mbar_wait(&bar->o_done, (n - 1) & 1, p.err, nullptr);
+      mma_commit(&bar->mma_done);
+      mbar_wait(&bar->mma_done, 0, p.err, nullptr);
     }
   } else {
     // ------------------------------------------------------------ softmax warps
-    const int q4 = warp & 3;               // TMEM lane quarter
-    const int hc = (warp - 2) >> 2;        // which 64 key columns (and O columns) this warp owns
-    const int r = q4 * 32 + lane;          // query row in the tile
+    const int x = (warp - 2) >> 2;  // tile of this warp group (0: A, 1: B)
+    const int nx = x == 0 ? nA : nB;
+    const int t = x == 0 ? tA : tB;
+    const int diag = diagA + x;
+    const int q4 = warp & 3;  // TMEM lane quarter
+    const int r = q4 * 32 + lane;  // query row in the tile
     const uint32_t lane_off = tmem_lane_base(warp);
-    const uint32_t tO = tmem + lane_off + 256 + hc * 64;
+    const uint32_t tS = tmem + lane_off + x * 128;
+    const uint32_t tO = tmem + lane_off + 256 + x * 128;
     const int qrow = t * kTile + r;
-    const int bar_id = 1 + q4;             // named barrier of the two warps sharing this quarter
     float m = -INFINITY, l = 0.f;
     bool ok = true;
-    // On an abort every thread still runs all named barriers (only the work is skipped),
-    // so the two warps of a pair can never wait on each other forever.
-    for (int j = 0; j < n; ++j) {
+    for (int j = 0; j < nx; ++j) {
       const int pg = p.sel[(size_t)h * p.max_sel + j];
-      const int b = j & 1;
-      const uint32_t tS = tmem + lane_off + b * 128;
-      uint32_t sr[64];
-      float my_max = -INFINITY;
-      if (ok) ok = mbar_wait(&bar->s_full[b], (j >> 1) & 1, p.err, abort);
+      if (ok) ok = mbar_wait(&bar->s_full[x], j & 1, p.err, abort);
       ok = __all_sync(0xffffffffu, ok);  // TMEM loads and stores below are warp-collective
-      if (ok) {
-        tc_fence_after();
-        tmem_ld32(tS + hc * 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-        tmem_ld32(tS + hc * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-        tmem_wait_ld();
-        if (pg == diag) {  // causal mask: key column c visible to row r iff c <= r
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sr[128];
 #pragma unroll
-          for (int c = 0; c < 64; ++c)
-            if (hc * 64 + c > r) sr[c] = 0xff800000u;  // -inf
-        }
-        float mx[8];
+      for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+      tmem_wait_ld();
+      if (pg == diag) {  // causal mask: key column c visible to row r iff c <= r
 #pragma unroll
-        for (int k = 0; k < 8; ++k) mx[k] = __uint_as_float(sr[k]);
-#pragma unroll
-        for (int c = 8; c < 64; c += 8)
-#pragma unroll
-          for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], __uint_as_float(sr[c + k]));
-        my_max = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        for (int c = 0; c < 128; ++c)
+          if (c > r) sr[c] = 0xff800000u;  // -inf
       }
-      // exchange the partial maxima; both threads of a row then take the same decisions.
-      // The barrier also orders this pair's S reads before either writes P over S.
-      bar->xchg[hc][r] = my_max;
-      named_bar_sync(bar_id, 64);
-      const float tmax = fmaxf(my_max, bar->xchg[hc ^ 1][r]) * p.scale_log2;
-      named_bar_sync(bar_id, 64);  // both have read before the slot is reused
-      if (!ok) continue;
+      float mx[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mx[k] = __uint_as_float(sr[k]);
+#pragma unroll
+      for (int c = 8; c < 128; c += 8)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], __uint_as_float(sr[c + k]));
+      const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) *
+                         p.scale_log2;
       bool rescale_o = false;
       float alpha = 1.f;
       if (tmax > m + kRescaleThreshold || (m == -INFINITY && tmax > -INFINITY)) {
@@ -298,26 +324,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float neg_m = (m == -INFINITY) ? 0.f : -m;
       float sum[4] = {0.f, 0.f, 0.f, 0.f};
-      uint32_t pk[32];
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
+      for (int c = 0; c < 64; ++c) {
         const float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * c]), p.scale_log2, neg_m));
         const float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * c + 1]), p.scale_log2, neg_m));
         sum[c & 3] += p0 + p1;
-        pk[c] = pack_bf16x2(p0, p1);
+        sr[c] = pack_bf16x2(p0, p1);  // packed P: key columns 2c, 2c+1 -> column c
       }
       l += (sum[0] + sum[1]) + (sum[2] + sum[3]);
-      if (j > 0) {  // PV of the previous page is done: O may be rescaled
-        ok = __all_sync(0xffffffffu, mbar_wait(&bar->o_done, (j - 1) & 1, p.err, abort));
-        if (!ok) continue;
-        tc_fence_after();
-      }
       // The rescale is decided per row but the TMEM accesses are warp-collective: the warp
       // rescales when any of its rows needs it, the other rows scale by alpha = 1 (exact).
       if (__any_sync(0xffffffffu, rescale_o)) {
         if (!rescale_o) alpha = 1.f;
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar->o_done[x], (j - 1) & 1, p.err, abort));  // PV_{j-1} done
+        if (!ok) break;
+        tc_fence_after();
 #pragma unroll 1
-        for (int cc = 0; cc < 2; ++cc) {
+        for (int cc = 0; cc < 4; ++cc) {
           uint32_t o[32];
           tmem_ld32(tO + cc * 32, o);
           tmem_wait_ld();
@@ -326,26 +349,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st32(tO + cc * 32, o);
         }
       }
-      tmem_st32(tS + hc * 32, pk);  // packed P: key columns 2c, 2c+1 of this half -> column 32 hc + c
+      tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&bar->p_full[b]);
+      mbar_arrive(&bar->p_full[x]);
     }
-    // epilogue: combine the pair's partial row sums, normalise this thread's 64 columns of O
-    bar->xchg[hc][r] = l;
-    named_bar_sync(bar_id, 64);
-    const float l_row = l + bar->xchg[hc ^ 1][r];
+    // epilogue: normalise this thread's row of O
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.o);
-    if (__all_sync(0xffffffffu, ok && n > 0 && mbar_wait(&bar->o_done, (n - 1) & 1, p.err, abort))) {
+    const bool have = x == 0 || hasB;
+    if (__all_sync(0xffffffffu, ok && nx > 0 && mbar_wait(&bar->o_done[x], (nx - 1) & 1, p.err, abort))) {
       tc_fence_after();
-      const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
-      for (int cc = 0; cc < 2; ++cc) {
+      for (int cc = 0; cc < 4; ++cc) {
         uint32_t o[32];
         tmem_ld32(tO + cc * 32, o);
         tmem_wait_ld();
         if (qrow < p.n_q) {
-          uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)qrow * p.Hq + hq) * kD + hc * 64 + cc * 32);
+          uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)qrow * p.Hq + hq) * kD + cc * 32);
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
             uint4 w;
@@ -357,11 +379,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (qrow < p.n_q && hc == 0) p.lse[(size_t)hq * p.n_q + qrow] = (m + log2f(l_row)) * kLn2;
-    } else if (qrow < p.n_q) {
-      uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)qrow * p.Hq + hq) * kD + hc * 64);
-      for (int v = 0; v < 8; ++v) dst[v] = make_uint4(0, 0, 0, 0);
-      if (hc == 0) p.lse[(size_t)hq * p.n_q + qrow] = -INFINITY;
+      if (qrow < p.n_q) p.lse[(size_t)hq * p.n_q + qrow] = (m + log2f(l)) * kLn2;
+    } else if (have && qrow < p.n_q) {
+      uint4* dst = reinterpret_cast<uint4*>(out + ((size_t)qrow * p.Hq + hq) * kD);
+      for (int v = 0; v < 16; ++v) dst[v] = make_uint4(0, 0, 0, 0);
+      p.lse[(size_t)hq * p.n_q + qrow] = -INFINITY;
     }
   }
   tc_fence_before();
@@ -403,12 +425,13 @@ cudaError_t launch_attn_fwd_tc(const AttnArgs& a, cudaStream_t st) {
   p.num_phys = a.g.num_phys;
   p.max_logical = a.g.max_logical;
   p.n_tiles = (a.n_q + kTile - 1) / kTile;
+  p.n_pairs = (p.n_tiles + 1) / 2;
   p.q_start = a.q_start;
   p.scale_log2 = a.scale * kLog2e;
   p.staged = a.kv.staged;
   p.stage_h0 = a.kv.stage_h0;
   p.stage_stride = a.kv.stage_stride;
-  dim3 grid(a.g.Hq, p.n_tiles);
+  dim3 grid(a.g.Hq, p.n_pairs);
   attn_fwd_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, p);
   count_launches(1);
   return cudaGetLastError();
