@@ -25,6 +25,11 @@
 //   warps 2-5  softmax of tile A, warps 6-9 softmax of tile B: one thread per query
 //              row holding all 128 key columns.  Base-2 online softmax with lazy
 //              rescaling of O (only when the row max grows by more than 2^8).
+// The MMA issuer commits only "S_X(j) ready" per page (its tensor-pipe queue is a few
+// instructions deep, so every extra commit or wait between groups idles the pipe).
+// MMAs complete in issue order, so a softmax warp that has seen S_X(j) also knows
+// that PV_X(j-1) has finished (O may be rescaled) and, when its tile is the last
+// user of page j, that K_j and V_{j-1} are free: it releases those ring slots.
 // TMEM columns: S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512).
 #include "tc_common.cuh"
 
@@ -60,7 +65,7 @@ struct __align__(8) FwdBarriers {
   uint64_t v_empty[kVStages];
   uint64_t s_full[2];  // per tile: S_j in TMEM
   uint64_t p_full[2];  // per tile: P_j written over S_j (and O rescaled)
-  uint64_t o_done[2];  // per tile: PV_j finished
+  uint64_t o_done[2];  // per tile: its last PV finished
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
@@ -117,7 +122,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar->s_full[i], 1);
-      mbar_init(&bar->p_full[i], kGroupThreads);
+      mbar_init(&bar->p_full[i], kGroupThreads / 32);  // one arrival per softmax warp
       mbar_init(&bar->o_done[i], 1);
     }
     mbar_init(&bar->mma_done, 1);
@@ -173,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool progressed = false;
         if (jk < n) {
           const int ks = jk % kKStages;
-          if (jk < kKStages || mbar_try_wait(&bar->k_empty[ks], ((jk / kKStages) - 1) & 1)) {
+          if (jk < kKStages || mbar_test_wait(&bar->k_empty[ks], ((jk / kKStages) - 1) & 1)) {
             const int row = (int)(block_of(jk) * kTile);
             mbar_arrive_expect_tx(&bar->k_full[ks], kTileBytes);
             tma_load_2d(sm + kOffK + ks * kTileBytes, &tk, &bar->k_full[ks], 0, row);
@@ -184,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (jv < jk) {
           const int vs = jv % kVStages;
-          if (jv < kVStages || mbar_try_wait(&bar->v_empty[vs], ((jv / kVStages) - 1) & 1)) {
+          if (jv < kVStages || mbar_test_wait(&bar->v_empty[vs], ((jv / kVStages) - 1) & 1)) {
             const int row = (int)(block_of(jv) * kTile);
             mbar_arrive_expect_tx(&bar->v_full[vs], kTileBytes);
             tma_load_2d(sm + kOffV + vs * kTileBytes, &tv, &bar->v_full[vs], 0, row);
@@ -234,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t a = tmem + x * 128, o = tmem + 256 + x * 128;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) mma_ts(o, a + kk * 8, desc_mnmajor(aV, kk), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&bar->o_done[x]);
+        if (j == nt[x] - 1) mma_commit(&bar->o_done[x]);  // the tile's last PV
         return true;
       };
       // page 0: both S
@@ -243,7 +248,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         for (int x = 0; x < 2; ++x)
           if (0 < nt[x]) issue_s(x, 0);
-        mma_commit(&bar->k_empty[0]);
       }
       for (int j = 0; ok && j < n; ++j) {
         const int j1 = j + 1;
@@ -255,7 +259,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               v_waited = true;
             }
             ok = ok && issue_pv(x, j);
-            if (ok && (x == 1 || j >= nt[1])) mma_commit(&bar->v_empty[j % kVStages]);  // last PV of page j
           }
           if (ok && j1 < nt[x]) {  // S_X(j+1)
             if (!k_waited) {
@@ -263,10 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               k_waited = true;
               if (ok) tc_fence_after();
             }
-            if (ok) {
-              issue_s(x, j1);
-              if (x == 1 || j1 >= nt[1]) mma_commit(&bar->k_empty[j1 % kKStages]);  // last S of page j+1
-            }
+            if (ok) issue_s(x, j1);
           }
         }
       }
@@ -294,6 +294,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, ok);  // TMEM loads and stores below are warp-collective
       if (!ok) break;
       tc_fence_after();
+      // the last user of page j frees K_j and V_{j-1} (their MMAs precede S_X(j))
+      if ((warp & 3) == 2 && lane == 0 && (x == 1 || j >= nB)) {
+        mbar_arrive(&bar->k_empty[j % kKStages]);
+        if (j > 0) mbar_arrive(&bar->v_empty[(j - 1) % kVStages]);
+      }
       uint32_t sr[128];
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
@@ -334,11 +339,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       l += (sum[0] + sum[1]) + (sum[2] + sum[3]);
       // The rescale is decided per row but the TMEM accesses are warp-collective: the warp
       // rescales when any of its rows needs it, the other rows scale by alpha = 1 (exact).
-      if (__any_sync(0xffffffffu, rescale_o)) {
+      if (__any_sync(0xffffffffu, rescale_o)) {  // PV_{j-1} finished before S_j
         if (!rescale_o) alpha = 1.f;
-        ok = __all_sync(0xffffffffu, mbar_wait(&bar->o_done[x], (j - 1) & 1, p.err, abort));  // PV_{j-1} done
-        if (!ok) break;
-        tc_fence_after();
 #pragma unroll 1
         for (int cc = 0; cc < 4; ++cc) {
           uint32_t o[32];
@@ -353,12 +355,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&bar->p_full[x]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar->p_full[x]);
     }
     // epilogue: normalise this thread's row of O
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.o);
     const bool have = x == 0 || hasB;
-    if (__all_sync(0xffffffffu, ok && nx > 0 && mbar_wait(&bar->o_done[x], (nx - 1) & 1, p.err, abort))) {
+    if (__all_sync(0xffffffffu, ok && nx > 0 && mbar_wait(&bar->o_done[x], 0, p.err, abort))) {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1

@@ -47,12 +47,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Non-blocking probe of a phase (never suspends the thread, unlike try_wait).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 // Bounded wait; returns false (and sets kErrMbarTimeout) if the phase never flips
 // within ~2^31 SM cycles (about a second), or at once if another warp of the
 // block has already given up (*abort != 0).  A timed-out waiter raises *abort so
 // that every other waiter of the block leaves its loop quickly too.
+// A phase that has already completed is seen by a cheap test_wait first: try_wait
+// stalls the issuing thread for a few hundred cycles even then, which would leave the
+// tensor pipe idle when the waiter is the MMA issuer.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err,
                                           volatile int* abort = nullptr) {
+  if (mbar_test_wait(bar, parity)) return true;
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   for (uint32_t i = 1;; ++i) {
