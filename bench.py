@@ -138,6 +138,7 @@ class Step:
         self.lse = torch.empty((w.n_q_heads, C), dtype=torch.float32, device=dev)
         self.dq = [torch.empty_like(ch["q"]) for ch in self.chunks]
         self.fwd_events, self.bwd_events, self.app_events, self.sel_events = [], [], [], []
+        self.recompute_events, self.prefetch_events = [], []  # reverse-sweep forwards; offload copies
         self.side = torch.cuda.Stream(device=dev) if self.offload else None
 
     def run(self, record=False):
@@ -153,7 +154,7 @@ class Step:
             self._fwd(c, ch, start, n, record)
         for c in range(w.n_chunks - 1, -1, -1):
             start, n = w.chunk_bounds(c)
-            self._fwd(c, self.chunks[c], start, n, record)  # recompute (activations are not kept)
+            self._fwd(c, self.chunks[c], start, n, record, recompute=True)  # activations are not kept
             self._bwd(c, self.chunks[c], start, n, record)
 
     def run_offload(self, record=False):
@@ -170,13 +171,20 @@ class Step:
         def append_select(c):
             start, n = w.chunk_bounds(c)
             ch = self.chunks[c]
-            L.oomb_kv_append(h, ch["k"], ch["v"], start)
-            L.oomb_page_select(h, ch["q"], start, w.top_k, w.n_sink, self.sel[c], self.cnt[c], self.ws_sel)
+            self._timed(record, self.app_events, c, L.oomb_kv_append, h, ch["k"], ch["v"], start)
+            self._timed(record, self.sel_events, c, L.oomb_page_select, h, ch["q"], start, w.top_k, w.n_sink,
+                        self.sel[c], self.cnt[c], self.ws_sel)
 
         def prefetch(c, after):
             for e in after:
                 side.wait_event(e)
+            if record:
+                p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                p0.record(side)
             L.oomb_prefetch(h, self.sel[c], self.cnt[c], c % 2, stream=side)
+            if record:
+                p1.record(side)
+                self.prefetch_events.append((p0, p1, c))
             done = ev()
             done.record(side)
             return done
@@ -207,7 +215,7 @@ class Step:
             main.wait_event(pf[c])
             L.oomb_pool_set_stage(h, c % 2)
             start, n = w.chunk_bounds(c)
-            self._fwd(c, self.chunks[c], start, n, record)
+            self._fwd(c, self.chunks[c], start, n, record, recompute=True)
             self._bwd(c, self.chunks[c], start, n, record)
             used[c] = ev()
             used[c].record(main)
@@ -252,7 +260,7 @@ class Step:
             e1.record()
             self.bwd_events.append((e0, e1, c))
 
-    def _fwd(self, c, ch, start, n, record):
+    def _fwd(self, c, ch, start, n, record, recompute=False):
         L, torch = self.L, self.torch
         if record:
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -263,6 +271,8 @@ class Step:
         if record:
             e1.record()
             self.fwd_events.append((e0, e1, c))
+            if recompute:
+                self.recompute_events.append((e0, e1, c))
 
     def lse_tail(self, n):
         if not hasattr(self, "_lse_tail") or self._lse_tail.shape[1] != n:
@@ -496,6 +506,22 @@ def main():
     hbm_peak = peaks.get("hbm_gbs", 6783.0)
     value = job_throughput(credited, ms, world) / 1e12
     tokens_per_s = job_throughput(w.seq, ms, world)
+    rec_ms = sum(a.elapsed_time(b) for a, b, _ in step.recompute_events) / args.steps
+    kern_ms = sum(a.elapsed_time(b) for ev in (step.fwd_events, step.bwd_events, step.app_events, step.sel_events)
+                  for a, b, _ in ev) / args.steps
+    prefetch = None
+    if step.prefetch_events:
+        import torch as _t
+        esz = 2 if w.dtype == "bf16" else 4
+        cnt = step.cnt.cpu()
+        pf_bytes = {c: int(cnt[c].sum()) * w.page * w.head_dim * 2 * esz for c in range(w.n_chunks)}
+        pf_s = sum(a.elapsed_time(b) for a, b, _ in step.prefetch_events) * 1e-3
+        pf_b = sum(pf_bytes[c] for _, _, c in step.prefetch_events)
+        prefetch = {"gbs": round(pf_b / pf_s / 1e9, 1), "bytes_per_chunk_max": max(pf_bytes.values()),
+                    "link": "pinned host memory -> HBM staging (side stream)",
+                    "side_stream_ms_per_step": round(pf_s * 1e3 / args.steps, 3),
+                    "main_stream_kernel_ms_per_step": round(kern_ms, 3),
+                    "exposed_ms_per_step": round(max(0.0, ms - kern_ms), 3)}
 
     line = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": max(3, args.warmup), "ms_per_step": round(ms, 3), "higher_is_better": True,
@@ -507,6 +533,8 @@ def main():
                        "l2": "inputs larger than L2 (Q+dO alone exceed 129 MB)",
                        "attention_kernels": "tcgen05" if L.oomb_uses_tensor_cores(step.pool.handle) else "simt"},
             "tokens_per_s_per_layer": round(tokens_per_s, 1),
+            "tokens_per_s_per_layer_no_recompute": round(job_throughput(w.seq, ms - rec_ms, world), 1),
+            "recompute_ms_per_step": round(rec_ms, 3),
             "credited_tflop_per_step": credited / 1e12,
             "fwd_call_tflops": round(fwd_tflops, 2), "bwd_call_tflops": round(bwd_tflops, 2),
             "roofline": {"bound": "tensor", "kernel": "oomb_chunk_attn_bwd", "achieved": round(bwd_tflops, 2),
@@ -523,6 +551,7 @@ def main():
                             "frac_of_hbm": round(sel_gbs / hbm_peak, 3) if sel_gbs else None,
                             "same_size_read_gbs": round(sel_ref, 1) if sel_ref else None,
                             "frac_of_same_size_read": round(sel_gbs / sel_ref, 3) if sel_ref else None},
+            "prefetch_call": prefetch,
             "gpu_launches": int(launches),
             "clocks": clk.summary()}
 

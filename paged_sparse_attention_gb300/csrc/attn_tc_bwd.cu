@@ -124,9 +124,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar->s_full[i], 1);
-      mbar_init(&bar->p_full[i], kSoftmaxThreads);
+      mbar_init(&bar->p_full[i], kSoftmaxThreads / 32);  // one arrival per softmax warp
       mbar_init(&bar->dq_full[i], 1);
-      mbar_init(&bar->dq_free[i], 128);
+      mbar_init(&bar->dq_free[i], 4);                    // one arrival per read-out warp
     }
     mbar_init(&bar->acc_full, 1);
     bar->abort = 0;
@@ -299,7 +299,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_st();
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(&bar->p_full[hh]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar->p_full[hh]);
       }
     }
     // epilogue: this CTA's rows of the gradient pool += scale * dK, dV (64 columns per thread)
@@ -353,7 +354,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(tmem + lane_off + hh * 128 + 96, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
           tmem_wait_ld();
           tc_fence_before();
-          mbar_arrive(&bar->dq_free[hh]);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar->dq_free[hh]);
         }
         const int q0 = t * kTile + hh * kHalf;
 #pragma unroll
