@@ -303,6 +303,26 @@ class Step:
         return out
 
 
+def recorded_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch of `kernel` from an ncu capture recorded in
+    profiles/traffic.txt, or None when there is none for this workload or the
+    kernel's source has changed since (its sha256 prefix no longer matches)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    for line in open(path):
+        f = line.split()
+        if len(f) < 5 or line.startswith("#") or f[0] != workload or f[1] != kernel:
+            continue
+        src = os.path.join(ROOT, f[2])
+        if not os.path.exists(src):
+            return None
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        return int(f[4]) if digest.startswith(f[3]) else None
+    return None
+
+
 def same_size_gbs(nbytes: int, dev, kind: str) -> float:
     """Bandwidth of a plain PyTorch kernel moving the same bytes from cold L2: a sum
     over nbytes (kind "read") or a copy of nbytes / 2 (kind "copy", nbytes moved in
@@ -540,7 +560,8 @@ def main():
             "roofline": {"bound": "tensor", "kernel": "oomb_chunk_attn_bwd", "achieved": round(bwd_tflops, 2),
                          "peak": peak, "unit": "TFLOP/s", "frac": round(bwd_tflops / peak, 4),
                          "peak_source": peaks.get("source", "") + " (bf16 dense, sustained)",
-                         "traffic": None},
+                         "traffic": recorded_traffic(w.name, "oomb_chunk_attn_bwd"),
+                         "traffic_unit": "DRAM bytes per launch (ncu dram__bytes_read.sum + write.sum)"},
             "append_call": {"gbs": round(app_gbs, 1) if app_gbs else None,
                             "frac_of_hbm": round(app_gbs / hbm_peak, 3) if app_gbs else None,
                             "same_size_copy_gbs": round(app_ref, 1) if app_ref else None,
