@@ -15,8 +15,8 @@
 //                  dS^T = P^T (dP^T - D)
 //                  dV  += P^T dO_h      dK  += dS^T Q_h          (A operands from TMEM)
 //                  dQ^T = K^T dS^T      (dS^T also written to shared memory as the B
-//                                        operand; dQ^T read out, staged and bulk-added
-//                                        to the fp32 accumulator in global memory)
+//                                        operand; dQ^T read out of TMEM and added
+//                                        to the fp32 accumulator with global reductions)
 //                and finally adds scale*dK and dV into the block's own rows of the
 //                fp32 gradient pool: no two CTAs own the same rows, so dK/dV need no
 //                atomics.
@@ -44,8 +44,6 @@ constexpr uint32_t kHalfTile = kHalf * kD * 2;  // 16 KB: one 64-row half tile (
 constexpr uint32_t kHalfBox = kHalfTile / 2;
 constexpr int kThreads = 448;
 constexpr int kSoftmaxThreads = 256;
-constexpr int kPieceRows = 16;                   // dQ rows per bulk reduce
-constexpr uint32_t kPieceBytes = kPieceRows * kD * 4;
 
 struct BwdParams {
   const int32_t* sel;
@@ -81,8 +79,7 @@ constexpr uint32_t kOffK = 0;
 constexpr uint32_t kOffV = kOffK + kTileBytes;
 constexpr uint32_t kOffRing = kOffV + kTileBytes;                 // kRing x (Q half, dO half)
 constexpr uint32_t kOffDS = kOffRing + kRing * 2 * kHalfTile;     // 2 x dS^T half [128 keys][64 q]
-constexpr uint32_t kOffStage = kOffDS + 2 * kHalfTile;            // 2 x dQ pieces
-constexpr uint32_t kOffVec = kOffStage + 2 * kPieceBytes;         // kRing x (lse2[64], D[64])
+constexpr uint32_t kOffVec = kOffDS + 2 * kHalfTile;              // kRing x (lse2[64], D[64])
 constexpr uint32_t kOffBar = kOffVec + kRing * 2 * kHalf * 4;
 constexpr size_t kSmemBytes = 1024 + kOffBar + sizeof(BwdBarriers);
 
@@ -334,54 +331,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------------ dQ read-out
+    // Each thread holds one head-dim column of dQ^T for the half's 64 query rows and adds
+    // it into the fp32 accumulator with global reductions: for a given row the warp's 32
+    // lanes cover 32 consecutive columns (one 128-byte line), and no shared memory is used.
     const int col = (warp & 3) * 32 + lane;  // head-dim column == TMEM lane of dQ^T
     const uint32_t lane_off = tmem_lane_base(warp);
-    const bool leader = (warp == 10 && lane == 0);
-    float* stage = reinterpret_cast<float*>(sm + kOffStage);
     bool ok = true;
-    int piece = 0;
-    // On an abort every thread still runs all named barriers (only the work is skipped).
-    for (int u = 0; u < n_steps; ++u) {
+    for (int u = 0; ok && u < n_steps; ++u) {
       const int t = t0 + u / p.G, g = u % p.G;
       const int hq = h * p.G + g;
       for (int hh = 0; hh < 2; ++hh) {
         uint32_t r[64];
-        if (ok) ok = mbar_wait(&bar->dq_full[hh], u & 1, p.err, abort);
-        ok = __all_sync(0xffffffffu, ok);
-        if (ok) {
-          tc_fence_after();
-          tmem_ld32(tmem + lane_off + hh * 128 + 64, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-          tmem_ld32(tmem + lane_off + hh * 128 + 96, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
-          tmem_wait_ld();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bar->dq_free[hh]);
-        }
+        ok = __all_sync(0xffffffffu, mbar_wait(&bar->dq_full[hh], u & 1, p.err, abort));
+        if (!ok) break;
+        tc_fence_after();
+        tmem_ld32(tmem + lane_off + hh * 128 + 64, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+        tmem_ld32(tmem + lane_off + hh * 128 + 96, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar->dq_free[hh]);  // dQ^T is in registers: its columns are free
         const int q0 = t * kTile + hh * kHalf;
+        const int nrows = min(kHalf, p.n_q - q0);
+        float* dst = p.dq_acc + ((size_t)hq * p.n_q + q0) * kD + col;
 #pragma unroll
-        for (int pc = 0; pc < kHalf / kPieceRows; ++pc, ++piece) {
-          const int buf = piece & 1;
-          if (leader) bulk_wait_read<1>();  // the reduce that last read this buffer is done
-          named_bar_sync(1, 128);
-          float* st = stage + buf * (kPieceRows * kD);
-          if (ok) {
-#pragma unroll
-            for (int rr = 0; rr < kPieceRows; ++rr) st[rr * kD + col] = __uint_as_float(r[pc * kPieceRows + rr]);
-          }
-          fence_proxy_async_smem();
-          named_bar_sync(1, 128);
-          if (leader && ok) {
-            const int r0 = q0 + pc * kPieceRows;
-            const int nrows = min(kPieceRows, p.n_q - r0);
-            if (nrows > 0) {
-              bulk_reduce_add_f32(p.dq_acc + ((size_t)hq * p.n_q + r0) * kD, st, (uint32_t)nrows * kD * 4);
-            }
-            bulk_commit();
-          }
-        }
+        for (int rr = 0; rr < kHalf; ++rr)
+          if (rr < nrows) atomicAdd(dst + (size_t)rr * kD, __uint_as_float(r[rr]));
       }
     }
-    if (leader) bulk_wait<0>();
   }
   tc_fence_before();
   __syncthreads();
