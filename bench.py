@@ -136,22 +136,42 @@ class Step:
         self.cnt = torch.zeros((w.n_chunks, w.n_kv_heads), dtype=torch.int32, device=dev)
         self.o = torch.empty((C, w.n_q_heads, w.head_dim), dtype=w.torch_dtype, device=dev)
         self.lse = torch.empty((w.n_q_heads, C), dtype=torch.float32, device=dev)
+        self.ob = [self.o]
+        self.lseb = [self.lse]
+        self.o_keep, self.lse_keep = {}, {}  # forward-sweep outputs, kept only for the no-recompute variant
         self.dq = [torch.empty_like(ch["q"]) for ch in self.chunks]
         self.fwd_events, self.bwd_events, self.app_events, self.sel_events = [], [], [], []
         self.recompute_events, self.prefetch_events = [], []  # reverse-sweep forwards; offload copies
         self.side = torch.cuda.Stream(device=dev) if self.offload else None
 
-    def run(self, record=False):
+    def run(self, record=False, no_recompute=False):
+        """One step.  The reverse sweep recomputes each chunk's O and LSE (activations are
+        not kept).  With no_recompute the forward sweep's outputs are kept per chunk and
+        the reverse sweep only runs the backward (the variant without recomputation)."""
         if self.offload:
             return self.run_offload(record)
-        L, w, h = self.L, self.w, self.pool.handle
+        L, w, h, torch = self.L, self.w, self.pool.handle, self.torch
         L.oomb_pool_reset(h)
         for c, ch in enumerate(self.chunks):
             start, n = w.chunk_bounds(c)
             self._timed(record, self.app_events, c, L.oomb_kv_append, h, ch["k"], ch["v"], start)
             self._timed(record, self.sel_events, c, L.oomb_page_select, h, ch["q"], start, w.top_k, w.n_sink,
                         self.sel[c], self.cnt[c], self.ws_sel)
-            self._fwd(c, ch, start, n, record)
+            if no_recompute:
+                if c not in self.o_keep:
+                    self.o_keep[c] = torch.empty_like(ch["q"])
+                    self.lse_keep[c] = torch.empty((w.n_q_heads, n), dtype=torch.float32, device=self.dev)
+                L.oomb_chunk_attn_fwd(h, ch["q"], start, self.sel[c], self.cnt[c], self.scale, self.o_keep[c],
+                                      self.lse_keep[c])
+            else:
+                self._fwd(c, ch, start, n, record)
+        if no_recompute:
+            for c in range(w.n_chunks - 1, -1, -1):
+                start, n = w.chunk_bounds(c)
+                ch = self.chunks[c]
+                L.oomb_chunk_attn_bwd(h, ch["q"], self.o_keep[c], ch["do"], self.lse_keep[c], start, self.sel[c],
+                                      self.cnt[c], self.scale, self.dq[c], self.ws_bwd)
+            return
         for c in range(w.n_chunks - 1, -1, -1):
             start, n = w.chunk_bounds(c)
             self._fwd(c, self.chunks[c], start, n, record, recompute=True)  # activations are not kept
@@ -248,36 +268,40 @@ class Step:
                        + 2 * cand * w.n_kv_heads * 4) if scored else 0) + w.n_kv_heads * w.max_sel * 4
         return app, sel
 
-    def _bwd(self, c, ch, start, n, record):
+    def _bwd(self, c, ch, start, n, record, buf=0):
         L, torch, w = self.L, self.torch, self.w
         if record:
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
-        lse = self.lse if n == w.chunk else self.lse_tail(n)
-        L.oomb_chunk_attn_bwd(self.pool.handle, ch["q"], self.o[:n], ch["do"], lse, start, self.sel[c],
+        lse = self.lseb[buf] if n == w.chunk else self.lse_tail(n, buf)
+        L.oomb_chunk_attn_bwd(self.pool.handle, ch["q"], self.ob[buf][:n], ch["do"], lse, start, self.sel[c],
                               self.cnt[c], self.scale, self.dq[c], self.ws_bwd)
         if record:
             e1.record()
             self.bwd_events.append((e0, e1, c))
 
-    def _fwd(self, c, ch, start, n, record, recompute=False):
+    def _fwd(self, c, ch, start, n, record, recompute=False, buf=0):
         L, torch = self.L, self.torch
         if record:
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record()
-        lse = self.lse if n == self.w.chunk else self.lse_tail(n)
+        lse = self.lseb[buf] if n == self.w.chunk else self.lse_tail(n, buf)
         L.oomb_chunk_attn_fwd(self.pool.handle, ch["q"], start, self.sel[c], self.cnt[c], self.scale,
-                              self.o[:n], lse)
+                              self.ob[buf][:n], lse)
         if record:
             e1.record()
             self.fwd_events.append((e0, e1, c))
             if recompute:
                 self.recompute_events.append((e0, e1, c))
 
-    def lse_tail(self, n):
-        if not hasattr(self, "_lse_tail") or self._lse_tail.shape[1] != n:
-            self._lse_tail = self.torch.empty((self.w.n_q_heads, n), dtype=self.torch.float32, device=self.dev)
-        return self._lse_tail
+    def lse_tail(self, n, buf=0):
+        if not hasattr(self, "_lse_tail"):
+            self._lse_tail = {}
+        t = self._lse_tail.get(buf)
+        if t is None or t.shape[1] != n:
+            t = self._lse_tail[buf] = self.torch.empty((self.w.n_q_heads, n), dtype=self.torch.float32,
+                                                       device=self.dev)
+        return t
 
     def pairs_per_chunk(self):
         """Selected, causally visible (query, key) pairs summed over query heads, per chunk."""
@@ -527,6 +551,17 @@ def main():
     value = job_throughput(credited, ms, world) / 1e12
     tokens_per_s = job_throughput(w.seq, ms, world)
     rec_ms = sum(a.elapsed_time(b) for a, b, _ in step.recompute_events) / args.steps
+    nr_ms = None
+    if not step.offload:  # the variant without recompute, timed directly (forward outputs kept per chunk)
+        step.run(no_recompute=True)
+        torch.cuda.synchronize()
+        n0, n1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n0.record()
+        for _ in range(args.steps):
+            step.run(no_recompute=True)
+        n1.record()
+        torch.cuda.synchronize()
+        nr_ms = reduce_max_ms(n0.elapsed_time(n1) / args.steps, world, dev)
     kern_ms = sum(a.elapsed_time(b) for ev in (step.fwd_events, step.bwd_events, step.app_events, step.sel_events)
                   for a, b, _ in ev) / args.steps
     prefetch = None
@@ -553,8 +588,9 @@ def main():
                        "l2": "inputs larger than L2 (Q+dO alone exceed 129 MB)",
                        "attention_kernels": "tcgen05" if L.oomb_uses_tensor_cores(step.pool.handle) else "simt"},
             "tokens_per_s_per_layer": round(tokens_per_s, 1),
-            "tokens_per_s_per_layer_no_recompute": round(job_throughput(w.seq, ms - rec_ms, world), 1),
-            "recompute_ms_per_step": round(rec_ms, 3),
+            "tokens_per_s_per_layer_no_recompute": round(job_throughput(w.seq, nr_ms, world), 1) if nr_ms else None,
+            "ms_per_step_no_recompute": round(nr_ms, 3) if nr_ms else None,
+            "recompute_call_ms_per_step": round(rec_ms, 3),
             "credited_tflop_per_step": credited / 1e12,
             "fwd_call_tflops": round(fwd_tflops, 2), "bwd_call_tflops": round(bwd_tflops, 2),
             "roofline": {"bound": "tensor", "kernel": "oomb_chunk_attn_bwd", "achieved": round(bwd_tflops, 2),
