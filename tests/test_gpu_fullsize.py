@@ -7,7 +7,10 @@ oracle recomputes sampled outputs for KV group 0:
     block of 256 rows; dK/dV of the chunk's own pages, which no other chunk
     touches (exact from the full-chunk O and LSE and the own-page keys alone);
   * sparse128k: the page selection of sampled chunks (exact up to near-ties) and
-    the forward of the last chunk on the oracle's own selection.
+    the forward of the last chunk on the oracle's own selection;
+  * sparse1m (inputs generated on the device, as the benchmark does): the last
+    chunk's selection over all 8063 candidates and the forward of its first and
+    last 128 rows on the oracle's selection.
 """
 import math
 import os
@@ -125,4 +128,55 @@ def test_sparse128k_selection_and_forward_fullsize():
     L.oomb_chunk_attn_fwd(step.pool.handle, step.chunks[c]["q"], start, sel, cnt, step.scale, o, lse)
     Oo, Lo = O.chunk_attn_fwd(pool, q, start, ref, 1.0 / math.sqrt(w.head_dim))
     assert O.rel_l2(f64(o[:, :G]), Oo) < 1e-2 and O.rel_l2(f64(lse[:G]), Lo) < 1e-2
+    step.pool.close()
+
+
+@pytest.mark.slow
+def test_sparse1m_last_chunk_fullsize():
+    """1M tokens in chunks of 8192, top-128: the full step as bench.Step runs it (inputs
+    generated on the device), then KV group 0 of the last chunk against the oracle:
+    the page selection over all 8063 candidates (exact up to near-ties; planted pages
+    kept) and the forward on the oracle's selection for the chunk's first and last
+    128 rows (the rows with the fewest and the most visible keys)."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_sparse_attention_gb300 import build
+    build.build()
+    w = synth.WORKLOADS["sparse1m"]
+    dev = torch.device("cuda")
+    step = bench.Step(w, dev)
+    step.run()
+    torch.cuda.synchronize()
+    assert L.oomb_check(step.pool.handle) == 0
+    S, G = w.n_chunks, w.group
+    order = synth.page_order(w).tolist()
+    pool = O.OraclePool(1, w.head_dim, w.page, w.num_phys, w.n_pages)
+    used = 0
+    for c in range(S):
+        start, n = w.chunk_bounds(c)
+        ch = step.chunks[c]
+        npg = -(-n // w.page)
+        pool.append(ch["k"][:, 0:1].double().cpu().numpy(), ch["v"][:, 0:1].double().cpu().numpy(), start,
+                    order[used:used + npg])
+        used += npg
+    c = S - 1
+    start, n = w.chunk_bounds(c)
+    q = step.chunks[c]["q"][:, :G].double().cpu().numpy()
+    ref = O.select_pages(pool, q, start, w.top_k, w.n_sink)
+    cand, scores = O.page_scores(pool, q, start, w.n_sink)
+    got = step.sel[c, 0, : int(step.cnt[c, 0])].cpu().numpy()
+    ok, swaps = O.near_tie_ok(got, ref[0], cand, scores[0], w.top_k)
+    assert ok, (got[:8], ref[0][:8])
+    plants = synth.PlantTable(w)
+    for p in plants.planted.get((c, 0), []):
+        assert p in set(got.tolist())
+    sel, cnt = pad_sel([ref[0]] * w.n_kv_heads, w.max_sel, dev)
+    o = torch.empty_like(step.chunks[c]["q"])
+    lse = torch.empty(w.n_q_heads, n, dtype=torch.float32, device=dev)
+    L.oomb_chunk_attn_fwd(step.pool.handle, step.chunks[c]["q"], start, sel, cnt, step.scale, o, lse)
+    torch.cuda.synchronize()
+    for r0 in (0, n - 128):
+        Oo, Lo = O.chunk_attn_fwd(pool, q[r0:r0 + 128], start + r0, ref, 1.0 / math.sqrt(w.head_dim))
+        assert O.rel_l2(f64(o[r0:r0 + 128, :G]), Oo) < 1e-2, r0
+        assert O.rel_l2(f64(lse[:G, r0:r0 + 128]), Lo) < 1e-2, r0
     step.pool.close()
