@@ -578,7 +578,31 @@ def main():
         pf_bytes = {c: int(cnt[c].sum()) * w.page * w.head_dim * 2 * esz for c in range(w.n_chunks)}
         pf_s = sum(a.elapsed_time(b) for a, b, _ in step.prefetch_events) * 1e-3
         pf_b = sum(pf_bytes[c] for _, _, c in step.prefetch_events)
-        prefetch = {"gbs": round(pf_b / pf_s / 1e9, 1), "bytes_per_chunk_max": max(pf_bytes.values()),
+        # isolated: the gather of the last chunks alone, and a plain pinned-host -> HBM copy
+        iso = []
+        for c in range(max(0, w.n_chunks - 3), w.n_chunks):
+            torch.cuda.synchronize()
+            g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            g0.record()
+            L.oomb_prefetch(step.pool.handle, step.sel[c], step.cnt[c], 0)
+            g1.record()
+            torch.cuda.synchronize()
+            iso.append(pf_bytes[c] / (g0.elapsed_time(g1) * 1e-3) / 1e9)
+        hbuf = torch.empty(256 << 20, dtype=torch.uint8).pin_memory()
+        dbuf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        dbuf.copy_(hbuf)
+        torch.cuda.synchronize()
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record()
+        for _ in range(4):
+            dbuf.copy_(hbuf, non_blocking=True)
+        c1.record()
+        torch.cuda.synchronize()
+        link = 4 * (256 << 20) / (c0.elapsed_time(c1) * 1e-3) / 1e9
+        prefetch = {"gbs_overlapped": round(pf_b / pf_s / 1e9, 1),
+                    "gbs_isolated": round(statistics.median(iso), 1),
+                    "host_link_copy_gbs": round(link, 1),
+                    "bytes_per_chunk_max": max(pf_bytes.values()),
                     "link": "pinned host memory -> HBM staging (side stream)",
                     "side_stream_ms_per_step": round(pf_s * 1e3 / args.steps, 3),
                     "main_stream_kernel_ms_per_step": round(kern_ms, 3),
@@ -598,6 +622,7 @@ def main():
             "ms_per_step_no_recompute": round(nr_ms, 3) if nr_ms else None,
             "recompute_call_ms_per_step": round(rec_ms, 3),
             "credited_tflop_per_step": credited / 1e12,
+            "value_frac_of_peak": round(value / peak, 4),
             "fwd_call_tflops": round(fwd_tflops, 2), "bwd_call_tflops": round(bwd_tflops, 2),
             "roofline": {"bound": "tensor", "kernel": "oomb_chunk_attn_bwd", "achieved": round(bwd_tflops, 2),
                          "peak": peak, "unit": "TFLOP/s", "frac": round(bwd_tflops / peak, 4),
