@@ -333,6 +333,20 @@ class Step:
         return out
 
 
+def state_bytes_per_10k(w) -> dict:
+    """Device bytes of one layer's attention state that grow with the context, per
+    10,000 tokens: K/V pools, fp32 dK/dV pools and the page summaries (the analogue,
+    for this path alone, of the pages' end-to-end memory growth per 10K tokens).
+    With offload the K/V pools live in host memory and only a fixed staging buffer is
+    on the device."""
+    esz = 2 if w.dtype == "bf16" else 4
+    per_tok_kv = 2 * w.n_kv_heads * w.head_dim * esz
+    per_tok_grad = 2 * w.n_kv_heads * w.head_dim * 4
+    per_tok_sum = w.n_kv_heads * w.head_dim * 4 / w.page
+    dev = per_tok_grad + per_tok_sum + (0 if w.offload else per_tok_kv)
+    return {"device": int(dev * 10000), "host": int(per_tok_kv * 10000) if w.offload else 0}
+
+
 def recorded_traffic(workload: str, kernel: str):
     """DRAM bytes per launch of `kernel` from an ncu capture recorded in
     profiles/traffic.txt, or None when there is none for this workload or the
@@ -623,6 +637,7 @@ def main():
             "recompute_call_ms_per_step": round(rec_ms, 3),
             "credited_tflop_per_step": credited / 1e12,
             "value_frac_of_peak": round(value / peak, 4),
+            "state_bytes_per_10k_tokens": state_bytes_per_10k(w),
             "fwd_call_tflops": round(fwd_tflops, 2), "bwd_call_tflops": round(bwd_tflops, 2),
             "roofline": {"bound": "tensor", "kernel": "oomb_chunk_attn_bwd", "achieved": round(bwd_tflops, 2),
                          "peak": peak, "unit": "TFLOP/s", "frac": round(bwd_tflops / peak, 4),
