@@ -425,13 +425,9 @@ size_t bwd_tc_workspace_bytes(const Geometry& g, int n_q) {
 }
 
 cudaError_t launch_attn_bwd_tc(const AttnArgs& a, cudaStream_t st) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static size_t smem_set[kMaxDevices] = {};
+  cudaError_t e = set_smem_limit((const void*)attn_bwd_tc_kernel, kSmemBytes, smem_set);
+  if (e != cudaSuccess) return e;
   const int n_pad = (a.n_q + kTile - 1) / kTile * kTile;
   char* ws = reinterpret_cast<char*>(a.ws);
   float* Dbuf = reinterpret_cast<float*>(ws);

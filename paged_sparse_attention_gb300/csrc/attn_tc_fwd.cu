@@ -402,13 +402,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 bool tc_supported(const Geometry& g) { return g.dtype == OOMB_BF16 && g.d == kD && g.P == kTile; }
 
 cudaError_t launch_attn_fwd_tc(const AttnArgs& a, cudaStream_t st) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static size_t smem_set[kMaxDevices] = {};
+  cudaError_t e = set_smem_limit((const void*)attn_fwd_tc_kernel, kSmemBytes, smem_set);
+  if (e != cudaSuccess) return e;
   CUtensorMap tq, tk, tv;
   if (!make_tmap_heads(&tq, a.q, a.n_q, a.g.Hq) || !make_tmap_rows(&tk, a.kv.k, kv_rows(a)) ||
       !make_tmap_rows(&tv, a.kv.v, kv_rows(a)))

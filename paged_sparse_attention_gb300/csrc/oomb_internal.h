@@ -80,6 +80,14 @@ __host__ __device__ inline size_t dtype_size(int dt) { return dt == OOMB_FP32 ? 
 // Count of kernel launches issued by the library (reported by oomb_launch_count).
 void count_launches(int n);
 
+// Per-device host caches (CUDA function attributes and device properties are per device).
+constexpr int kMaxDevices = 64;
+// Raises `fn`'s dynamic shared-memory limit to `bytes` on the current device, once per
+// device and size; `done` is the caller's [kMaxDevices] record of sizes already set.
+cudaError_t set_smem_limit(const void* fn, size_t bytes, size_t* done);
+// Number of SMs of the current device.
+int device_sm_count();
+
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 }  // namespace oomb

@@ -78,16 +78,6 @@ struct SelParams {
   uint32_t bar_base[kBarriers];  // counter values before this call
 };
 
-int num_sms() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
-  return n;
-}
 
 template <typename T>
 __device__ __forceinline__ float to_f(T x);
@@ -741,7 +731,7 @@ cudaError_t launch_page_select(const Geometry& g, const float* summary, const in
   }
   const int VEC = (int)(16 / dtype_size(g.dtype));
   if (g.G * g.d / VEC > kMaxSlots * kThreads) return cudaErrorInvalidValue;
-  const int grid = std::min(num_sms(), kMaxBlocks);
+  const int grid = std::min(device_sm_count(), kMaxBlocks);
   p.n_slices = std::max(1, grid / g.Hkv);
   p.rows_per_block = (n_q + p.n_slices - 1) / p.n_slices;
   p.pages_per_block = (p.n_cand + grid - 1) / grid;
@@ -756,11 +746,10 @@ cudaError_t launch_page_select(const Geometry& g, const float* summary, const in
   if (p.keys_in_smem) smem = std::max(smem, align_up((size_t)p.n_cand, 4) * sizeof(uint32_t));
   if (smem > 200 * 1024) return cudaErrorInvalidValue;
   // the default dynamic limit is 48 KB minus the static shared memory: always opt in
-  static size_t configured[2] = {0, 0};
-  if (smem > configured[bf16]) {
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static size_t smem_set[2][kMaxDevices] = {};
+  {
+    cudaError_t e = set_smem_limit(fn, smem, smem_set[bf16]);
     if (e != cudaSuccess) return e;
-    configured[bf16] = smem;
   }
   int per_sm = 0;
   cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, smem);
