@@ -593,15 +593,17 @@ def main():
         pf_s = sum(a.elapsed_time(b) for a, b, _ in step.prefetch_events) * 1e-3
         pf_b = sum(pf_bytes[c] for _, _, c in step.prefetch_events)
         # isolated: the gather of the last chunks alone, and a plain pinned-host -> HBM copy
-        iso = []
+        iso, iso_ms = [], []
         for c in range(max(0, w.n_chunks - 3), w.n_chunks):
-            torch.cuda.synchronize()
-            g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            g0.record()
-            L.oomb_prefetch(step.pool.handle, step.sel[c], step.cnt[c], 0)
-            g1.record()
-            torch.cuda.synchronize()
-            iso.append(pf_bytes[c] / (g0.elapsed_time(g1) * 1e-3) / 1e9)
+            for rep in range(3):
+                torch.cuda.synchronize()
+                g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                g0.record()
+                L.oomb_prefetch(step.pool.handle, step.sel[c], step.cnt[c], rep % 2)
+                g1.record()
+                torch.cuda.synchronize()
+                iso_ms.append(round(g0.elapsed_time(g1), 3))
+                iso.append(pf_bytes[c] / (iso_ms[-1] * 1e-3) / 1e9)
         hbuf = torch.empty(256 << 20, dtype=torch.uint8).pin_memory()
         dbuf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
         dbuf.copy_(hbuf)
@@ -615,6 +617,7 @@ def main():
         link = 4 * (256 << 20) / (c0.elapsed_time(c1) * 1e-3) / 1e9
         prefetch = {"gbs_overlapped": round(pf_b / pf_s / 1e9, 1),
                     "gbs_isolated": round(statistics.median(iso), 1),
+                    "isolated_call_ms": iso_ms,
                     "host_link_copy_gbs": round(link, 1),
                     "bytes_per_chunk_max": max(pf_bytes.values()),
                     "link": "pinned host memory -> HBM staging (side stream)",
