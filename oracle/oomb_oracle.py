@@ -190,6 +190,19 @@ def select_pages(pool: OraclePool, q: np.ndarray, q_start: int, top_k: int,
     return out
 
 
+def window_pages(q_start: int, n_q: int, page_size: int, window: int, n_sink: int) -> np.ndarray:
+    """Local sliding-window selection, the same for every KV head (explainer, 2.D
+    "Page-Level Sparse Attention": sparse-native models use local attention in
+    their sparse layers).  Reading: page granularity and no scoring; the chunk
+    keeps the sink pages, the ``window`` complete history pages right before it,
+    and its own pages.  Written as a set union, ascending."""
+    n_hist = q_start // page_size
+    own = set(range(n_hist, (q_start + n_q - 1) // page_size + 1))
+    sinks = set(range(0, min(n_sink, n_hist)))
+    recent = set(p for p in range(n_hist) if n_hist - p <= window)
+    return np.array(sorted(sinks | recent | own), dtype=np.int64)
+
+
 # -- attention -------------------------------------------------------------------
 def _row_softmax_stats(s: np.ndarray):
     """m, LSE and P of a masked logit matrix (masked entries are -inf)."""
@@ -255,12 +268,14 @@ def chunk_attn_bwd(pool: OraclePool, q: np.ndarray, o: np.ndarray, do: np.ndarra
 # -- whole sweep -----------------------------------------------------------------
 def chunked_sweep(chunks, phys_order: Sequence[int], n_kv_heads: int, page_size: int,
                   num_phys: int, scale: float, top_k: int = -1, n_sink: int = 1,
-                  sel_override=None):
+                  sel_override=None, window: Optional[int] = None):
     """Chunk-recurrent forward (in order) then backward (reverse order).
 
     ``chunks`` is a list of dicts with float64 arrays q/k/v/do.  Physical pages are
-    handed out in ``phys_order``.  Returns per-chunk O, LSE, dQ, selections and
-    the pool (whose dK/dV hold the accumulated key/value gradients).
+    handed out in ``phys_order``.  Pages are chosen by top-K retrieval, or by the
+    local window when ``window`` is given.  Returns per-chunk O, LSE, dQ,
+    selections and the pool (whose dK/dV hold the accumulated key/value
+    gradients).
     """
     d = chunks[0]["q"].shape[2]
     total = sum(c["q"].shape[0] for c in chunks)
@@ -277,8 +292,12 @@ def chunked_sweep(chunks, phys_order: Sequence[int], n_kv_heads: int, page_size:
         newp = order[next_free:next_free + (p1 - p0 + 1)]
         next_free += p1 - p0 + 1
         pool.append(c["k"], c["v"], start, newp)
-        sel = sel_override[ci] if sel_override is not None else \
-            select_pages(pool, c["q"], start, top_k, n_sink)
+        if sel_override is not None:
+            sel = sel_override[ci]
+        elif window is not None:
+            sel = [window_pages(start, n, page_size, window, n_sink)] * n_kv_heads
+        else:
+            sel = select_pages(pool, c["q"], start, top_k, n_sink)
         O, L = chunk_attn_fwd(pool, c["q"], start, sel, scale)
         res["O"].append(O)
         res["LSE"].append(L)

@@ -273,3 +273,82 @@ def test_near_tie_rule():
     scores = np.array([1.0, 0.5, 0.50000001, 0.2, 0.1])
     assert O.near_tie_ok(np.array([0, 1, 2]), np.array([0, 1, 3]), cand, scores, 2)[0]
     assert not O.near_tie_ok(np.array([0, 1, 4]), np.array([0, 1, 3]), cand, scores, 2)[0]
+
+
+# -- local sliding-window selection ------------------------------------------------
+def test_golden_handworked_window():
+    with open(os.path.join(GOLDEN, "window_handworked.json")) as f:
+        g = json.load(f)
+    for case in g["cases"]:
+        got = O.window_pages(case["q_start"], case["n_q"], g["page_size"], case["window"], case["n_sink"])
+        assert got.tolist() == case["expected"], case
+
+
+def _sdpa_masked(Q, K, V, dO, scale, mask):
+    """torch fp64 SDPA with an explicit boolean visibility mask [N, N] (library
+    routine), GQA by repeat_interleave; returns O and the gradients of sum(dO*O)."""
+    G = Q.shape[1] // K.shape[1]
+    tq = torch.tensor(Q.transpose(1, 0, 2), dtype=torch.float64, requires_grad=True)
+    tk = torch.tensor(K.transpose(1, 0, 2), dtype=torch.float64, requires_grad=True)
+    tv = torch.tensor(V.transpose(1, 0, 2), dtype=torch.float64, requires_grad=True)
+    to = torch.nn.functional.scaled_dot_product_attention(
+        tq[None], tk.repeat_interleave(G, 0)[None], tv.repeat_interleave(G, 0)[None],
+        attn_mask=torch.tensor(mask)[None, None], scale=scale)[0]
+    (to * torch.tensor(dO.transpose(1, 0, 2))).sum().backward()
+    t = lambda x: x.numpy().transpose(1, 0, 2)  # noqa: E731
+    return t(to.detach()), t(tq.grad), t(tk.grad), t(tv.grad)
+
+
+def _window_mask(N, C, P, window, n_sink):
+    """Token-level visibility written from the definition in words: query i sees
+    key j <= i when j lies in a sink page before i's chunk, in one of the `window`
+    pages right before i's chunk, or in i's own chunk."""
+    mask = np.zeros((N, N), dtype=bool)
+    for i in range(N):
+        first = (i // C) * C // P  # first page of i's chunk
+        for j in range(i + 1):
+            pj = j // P
+            mask[i, j] = (pj >= first) or (first - window <= pj) or (pj < min(n_sink, first))
+    return mask
+
+
+@pytest.mark.parametrize("N,C,P,Hq,Hkv,d,window,n_sink", [
+    (96, 32, 8, 4, 2, 8, 0, 0),     # chunk-local attention
+    (96, 32, 8, 4, 2, 8, 2, 1),
+    (100, 24, 4, 3, 1, 16, 3, 2),   # ragged last chunk
+    (64, 16, 4, 2, 2, 4, 100, 1),   # window covers the history: dense
+])
+def test_window_sweep_equals_masked_sdpa(N, C, P, Hq, Hkv, d, window, n_sink):
+    rng = np.random.default_rng(N + 7 * window + n_sink)
+    Q, K, V, dO = _rand_seq(rng, N, Hq, Hkv, d)
+    scale = 1.0 / math.sqrt(d)
+    order = rng.permutation(-(-N // P) + 2)
+    res = O.chunked_sweep(_split(Q, K, V, dO, C), order, Hkv, P, len(order), scale, n_sink=n_sink,
+                          window=window)
+    Ot, dQt, dKt, dVt = _sdpa_masked(Q, K, V, dO, scale, _window_mask(N, C, P, window, n_sink))
+    dK, dV = res["pool"].logical_grads()
+    assert O.rel_l2(_cat(res, "O"), Ot) < 1e-12
+    assert O.rel_l2(np.concatenate(res["dQ"]), dQt) < 1e-12
+    assert O.rel_l2(dK, dKt) < 1e-12
+    assert O.rel_l2(dV, dVt) < 1e-12
+    if window == 0 and n_sink == 0:  # block-diagonal: each chunk is plain causal attention on its own
+        for s in range(0, N, C):
+            Oc, _ = O.dense_causal_attention(Q[s:s + C], K[s:s + C], V[s:s + C], scale)
+            assert O.rel_l2(Ot[s:s + C], Oc) < 1e-12
+
+
+def test_window_off_by_one_is_caught(monkeypatch):
+    """A window one page too short must fail the masked-SDPA pin."""
+    N, C, P, Hq, Hkv, d = 64, 16, 4, 2, 1, 4
+    rng = np.random.default_rng(5)
+    Q, K, V, dO = _rand_seq(rng, N, Hq, Hkv, d)
+    good = O.window_pages
+
+    def short(q_start, n_q, page_size, window, n_sink):
+        return good(q_start, n_q, page_size, max(0, window - 1), n_sink)
+
+    monkeypatch.setattr(O, "window_pages", short)
+    res = O.chunked_sweep(_split(Q, K, V, dO, C), list(range(N // P)), Hkv, P, N // P, 0.5, n_sink=1, window=2)
+    monkeypatch.setattr(O, "window_pages", good)
+    Ot, _, _, _ = _sdpa_masked(Q, K, V, dO, 0.5, _window_mask(N, C, P, 2, 1))
+    assert O.rel_l2(_cat(res, "O"), Ot) > 1e-3
