@@ -159,8 +159,7 @@ class Step:
             if wait_in is not None:
                 torch.cuda.current_stream(self.dev).wait_event(wait_in[c])
             self._timed(record, self.app_events, c, L.oomb_kv_append, h, ch["k"], ch["v"], start)
-            self._timed(record, self.sel_events, c, L.oomb_page_select, h, ch["q"], start, w.top_k, w.n_sink,
-                        self.sel[c], self.cnt[c], self.ws_sel)
+            self._select(c, ch, start, n, record)
             if no_recompute:
                 if c not in self.o_keep:
                     self.o_keep[c] = torch.empty_like(ch["q"])
@@ -198,8 +197,7 @@ class Step:
             start, n = w.chunk_bounds(c)
             ch = self.chunks[c]
             self._timed(record, self.app_events, c, L.oomb_kv_append, h, ch["k"], ch["v"], start)
-            self._timed(record, self.sel_events, c, L.oomb_page_select, h, ch["q"], start, w.top_k, w.n_sink,
-                        self.sel[c], self.cnt[c], self.ws_sel)
+            self._select(c, ch, start, n, record)
 
         def prefetch(c, after):
             for e in after:
@@ -254,6 +252,16 @@ class Step:
         fn(*args)
         e1.record()
         events.append((e0, e1, c))
+
+    def _select(self, c, ch, start, n, record):
+        """Chunk c's pages: top-K retrieval, or the local window for window workloads."""
+        L, w, h = self.L, self.w, self.pool.handle
+        if w.window >= 0:
+            self._timed(record, self.sel_events, c, L.oomb_window_select, h, start, n, w.window, w.n_sink,
+                        self.sel[c], self.cnt[c])
+        else:
+            self._timed(record, self.sel_events, c, L.oomb_page_select, h, ch["q"], start, w.top_k, w.n_sink,
+                        self.sel[c], self.cnt[c], self.ws_sel)
 
     def hbm_bytes(self):
         """Algorithmic HBM bytes per call of append and select, per chunk."""
@@ -394,6 +402,36 @@ def same_size_gbs(nbytes: int, dev, kind: str) -> float:
     return (n * 4 * (1 if kind == "read" else 2)) / (times[len(times) // 2] * 1e-3) / 1e9
 
 
+def measure_graph(step, steps: int, world: int, dev) -> dict:
+    """The same step captured once in a CUDA graph and replayed: every library call
+    of the step (pool reset, append, selection, forward, recompute, backward) is a
+    node, so the host issues one launch per step.  Returns its step time, or why
+    the capture failed."""
+    import torch
+
+    import paged_sparse_attention_gb300 as L
+    try:
+        g = torch.cuda.CUDAGraph()
+        n0 = L.oomb_launch_count()
+        with torch.cuda.graph(g):
+            step.run()
+        per_step = L.oomb_launch_count() - n0
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = reduce_max_ms(e0.elapsed_time(e1) / steps, world, dev)
+        L.oomb_check(step.pool.handle)
+        return {"ms_per_step": round(ms, 3), "kernel_launches_per_step": per_step,
+                "note": "one CUDA graph per step, replayed; same work as the eager step"}
+    except Exception as e:  # report, do not hide: the eager numbers above stand on their own
+        return {"unavailable": f"{type(e).__name__}: {str(e).splitlines()[0][:200]}"}
+
+
 def reduce_max_ms(ms: float, world: int, device) -> float:
     """Step time of the whole job: the maximum over ranks (replicas run independently)."""
     if world <= 1:
@@ -435,7 +473,10 @@ def oracle_sample_seconds(w, budget_s=20.0):
     start, n = w.chunk_bounds(c)
     q = chunks[c]["q"][:, :G].double().numpy()
     do = chunks[c]["do"][:, :G].double().numpy()
-    sel = O.select_pages(pool, q, start, w.top_k, w.n_sink)
+    if w.window >= 0:
+        sel = [O.window_pages(start, n, w.page, w.window, w.n_sink)]
+    else:
+        sel = O.select_pages(pool, q, start, w.top_k, w.n_sink)
     scale = 1.0 / math.sqrt(w.head_dim)
     # credited pairs of the sample
     kpos = np.concatenate([p * w.page + np.arange(pool.tokens_in_page(p)) for p in sel[0]])
@@ -487,6 +528,7 @@ def main():
     ap.add_argument("--workload", default="dense32k")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
@@ -582,6 +624,7 @@ def main():
         n1.record()
         torch.cuda.synchronize()
         nr_ms = reduce_max_ms(n0.elapsed_time(n1) / args.steps, world, dev)
+    graph = None if step.offload or args.no_graph else measure_graph(step, args.steps, world, dev)
     kern_ms = sum(a.elapsed_time(b) for ev in (step.fwd_events, step.bwd_events, step.app_events, step.sel_events)
                   for a, b, _ in ev) / args.steps
     prefetch = None
@@ -630,6 +673,7 @@ def main():
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "fp32",
             "data": "synthetic (seeded N(0,1) Q/K/V/dO, RoPE theta 1e6; no trained weights)",
             "config": {"workload": w.name, "seq": w.seq, "chunk": w.chunk, "page": w.page, "top_k": w.top_k,
+                       **({"window_pages": w.window, "n_sink": w.n_sink} if w.window >= 0 else {}),
                        "heads": f"{w.n_q_heads}/{w.n_kv_heads}", "head_dim": w.head_dim,
                        "parallelism": "replicas" if world > 1 else "single",
                        "l2": "inputs larger than L2 (Q+dO alone exceed 129 MB)",
@@ -658,6 +702,8 @@ def main():
                             "same_size_read_gbs": round(sel_ref, 1) if sel_ref else None,
                             "frac_of_same_size_read": round(sel_gbs / sel_ref, 3) if sel_ref else None},
             "prefetch_call": prefetch,
+            "graph": (dict(graph, value=round(job_throughput(credited, graph["ms_per_step"], world) / 1e12, 3))
+                      if graph and "ms_per_step" in graph else graph),
             "gpu_launches": int(launches),
             "clocks": clk.summary()}
 

@@ -82,10 +82,13 @@ typedef enum { OOMB_OP_SELECT = 0, OOMB_OP_BWD = 1 } oomb_op;
 #define OOMB_DEVERR_TMEM 0x8u     /* tensor-memory allocation failed */
 
 /* Length of the pool's control block (oomb_pool_desc.error_word), in uint32.
- * Word 0 holds the error bits above; words 4..6 are the grid-barrier counters of
- * oomb_page_select, which only grow (the library keeps their expected values on
- * the host).  Because that state is per pool, page selections on one pool must
- * not run concurrently (issue them on one stream, or order them with events). */
+ * Word 0 holds the error bits above; words 4..5 are the grid-barrier counters of
+ * oomb_page_select.  Each barrier's arrivals add exactly 2^31 to its counter
+ * (sense reversal), so the counters return to a state with zero low 31 bits
+ * after every selection and the host keeps no barrier state: a selection can be
+ * captured in a CUDA graph and replayed.  The counters are per pool, so page
+ * selections on one pool must not run concurrently (issue them on one stream,
+ * or order them with events). */
 #define OOMB_CTRL_WORDS 16
 
 typedef struct {
@@ -150,7 +153,8 @@ OOMB_API oomb_status oomb_kv_append(oomb_pool* pool, const void* k, const void* 
  * OOMB_OP_SELECT, n_q) bytes of device memory, contents scratch.
  * Launch: one cooperative kernel (one CTA per SM) whose phases meet at grid
  * barriers kept in the pool's control block, so selections on one pool must be
- * ordered (one stream, or events).  A barrier wait that runs out (~1 s) sets
+ * ordered (one stream, or events).  No host state changes between calls, so the
+ * call may be captured in a CUDA graph.  A barrier wait that runs out (~1 s) sets
  * OOMB_DEVERR_TIMEOUT; oomb_check reports it and clears the control block.
  * Errors: ARG (incl. max_sel too small), ALIGN, WORKSPACE, CUDA. */
 OOMB_API oomb_status oomb_page_select(oomb_pool* pool, const void* q, int64_t q_start, int n_q, int top_k, int n_sink,
@@ -182,6 +186,25 @@ OOMB_API oomb_status oomb_page_select(oomb_pool* pool, const void* q, int64_t q_
 OOMB_API oomb_status oomb_page_select_noalloc(oomb_pool* pool, const void* q, int64_t q_start, int n_q, int top_k,
                                               int n_sink, int32_t* sel, int32_t* sel_count, int max_sel,
                                               void* stream);
+
+/* Local sliding-window selection, the "local attention" that the explainer (2.D
+ * "Page-Level Sparse Attention", native support for sparse-native models) pairs
+ * with top-K retrieval: the sparse layers of such a model attend only to the
+ * most recent context.  Page granularity, no scoring: with n_hist = q_start/P,
+ * every KV head gets
+ *     [0, min(n_sink, n_hist))                      sink pages (n_sink >= 0)
+ *   U [max(n_sink', n_hist - window), n_hist)       the window history pages
+ *                                                   right before the chunk
+ *   U [n_hist, ceil((q_start + n_q)/P))             the chunk's own pages
+ * ascending, in sel[h*max_sel ...] with the count in sel_count[h] (device,
+ * int32; entries past the count are left as they were).  Feed the result to
+ * oomb_chunk_attn_fwd/bwd (and oomb_prefetch) like a top-K selection.  Reads no
+ * K/V and no workspace; one small kernel on the stream.  q_start must be a
+ * multiple of P and the chunk's own K/V already appended.
+ * Errors: ARG (window < 0, n_sink < 0, max_sel smaller than the set), ALIGN,
+ * CUDA. */
+OOMB_API oomb_status oomb_window_select(oomb_pool* pool, int64_t q_start, int n_q, int window, int n_sink,
+                                        int32_t* sel, int32_t* sel_count, int max_sel, void* stream);
 
 /* Chunk attention forward.  For query head hq and row i (absolute position
  * q_start+i): keys = every token of the selected pages of KV head hq/G with

@@ -76,6 +76,7 @@ def load(path: str = LIB_PATH) -> C.CDLL:
         "oomb_uses_tensor_cores": (i32, [vp]),
         "oomb_launch_count": (C.c_uint64, []),
         "oomb_page_select_noalloc": (i32, [vp, vp, i64, i32, i32, i32, vp, vp, i32, vp]),
+        "oomb_window_select": (i32, [vp, i64, i32, i32, i32, vp, vp, i32, vp]),
         "oomb_last_cuda_error": (C.c_char_p, []),
     }
     for name, (res, args) in sig.items():
@@ -134,6 +135,12 @@ def oomb_page_select(pool: int, q, q_start: int, top_k: int, n_sink: int, sel, s
     _ok("oomb_page_select", load().oomb_page_select(pool, _ptr(q), q_start, n, top_k, n_sink, _ptr(sel),
                                                     _ptr(sel_count), sel.shape[-1], _ptr(workspace), ws_bytes,
                                                     _stream(stream)))
+
+
+def oomb_window_select(pool: int, q_start: int, n_q: int, window: int, n_sink: int, sel, sel_count,
+                       stream=None) -> None:
+    _ok("oomb_window_select", load().oomb_window_select(pool, q_start, n_q, window, n_sink, _ptr(sel),
+                                                        _ptr(sel_count), sel.shape[-1], _stream(stream)))
 
 
 def oomb_chunk_attn_fwd(pool: int, q, q_start: int, sel, sel_count, softmax_scale: float, o, lse,

@@ -17,7 +17,6 @@ struct oomb_pool {
   int64_t n_tokens = 0;
   int stage_buf = 0;
   bool table_dirty = true;  // device page table still needs its -1 fill
-  uint32_t bar_ctr[3] = {0, 0, 0};  // values of the selection kernel's barrier counters
 };
 
 namespace {
@@ -267,8 +266,26 @@ oomb_status oomb_page_select(oomb_pool* p, const void* q, int64_t q_start, int n
   if (!ws || ws_bytes < need) return OOMB_ERR_WORKSPACE;
   if (!aligned(ws, 16)) return OOMB_ERR_ALIGN;
   return cuda_status(launch_page_select(p->g, p->d.summary, p->d.page_table, q, q_start, n_q, top_k, n_sink, sel,
-                                        sel_count, max_sel, ws, p->d.error_word, p->d.error_word, p->bar_ctr,
+                                        sel_count, max_sel, ws, p->d.error_word, p->d.error_word,
                                         (cudaStream_t)stream));
+}
+
+oomb_status oomb_window_select(oomb_pool* p, int64_t q_start, int n_q, int window, int n_sink, int32_t* sel,
+                               int32_t* sel_count, int max_sel, void* stream) {
+  if (!p || !sel || !sel_count) return OOMB_ERR_ARG;
+  if (n_q <= 0 || q_start < 0 || max_sel <= 0 || window < 0 || n_sink < 0) return OOMB_ERR_ARG;
+  if (q_start % p->g.P != 0) return OOMB_ERR_ALIGN;
+  if (q_start + n_q > p->n_tokens) return OOMB_ERR_ARG;  // own K/V must be appended
+  if (!aligned(sel, 4) || !aligned(sel_count, 4)) return OOMB_ERR_ALIGN;
+  const int P = p->g.P;
+  const int64_t n_hist = q_start / P;
+  const int64_t own_end = (q_start + n_q + P - 1) / P;
+  const int64_t sinks = n_sink < n_hist ? n_sink : n_hist;
+  const int64_t lo = std::max<int64_t>(sinks, n_hist - window);
+  if (own_end > p->g.max_logical) return OOMB_ERR_ARG;
+  if (sinks + (own_end - lo) > max_sel) return OOMB_ERR_ARG;
+  return cuda_status(launch_window_select(p->g, (int)sinks, (int)lo, (int)own_end, sel, sel_count, max_sel,
+                                          (cudaStream_t)stream));
 }
 
 static AttnArgs make_args(oomb_pool* p, const void* q, int64_t q_start, int n_q, const int32_t* sel,
@@ -356,7 +373,6 @@ oomb_status oomb_check(oomb_pool* p, void* stream, uint32_t* bits_out) {
   // at a grid barrier may have left a counter behind
   if (e == cudaSuccess && bits) {
     e = cudaMemset(p->d.error_word, 0, OOMB_CTRL_WORDS * sizeof(uint32_t));
-    for (uint32_t& c : p->bar_ctr) c = 0;
   }
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (bits_out) *bits_out = bits;

@@ -50,6 +50,7 @@ constexpr size_t kSumBytesCap = 128 * 1024;  // summary rows staged per CTA (two
 constexpr long long kSpinLimit = 1ll << 31;
 constexpr int kCtrlCount = 4;          // control-block words 4..5: barrier counters
 constexpr int kBarriers = 2;
+static_assert(kCtrlCount + kBarriers <= OOMB_CTRL_WORDS, "barrier counters must fit the control block");
 static_assert(kThreads * 8 == kHistBins, "phase 4 gives every thread eight histogram bins");
 
 struct SelParams {
@@ -75,7 +76,6 @@ struct SelParams {
   int32_t* sel_count;
   uint32_t* err;
   uint32_t* ctrl;
-  uint32_t bar_base[kBarriers];  // counter values before this call
 };
 
 
@@ -101,24 +101,31 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
   asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
   return m;
 }
-__device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+__device__ __forceinline__ uint32_t atom_release_add(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.release.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
 }
 
-// Grid barrier i: every CTA adds one to counter i; a waiting CTA spins until the
-// counter has grown by gridDim.x since the call began.  Returns false when the
-// wait ran out (~1 s), after setting the timeout bit.
+// Grid barrier i, sense-reversing: CTA 0 adds 2^31 - (gridDim.x - 1) to counter i
+// and every other CTA adds 1, so one barrier's arrivals sum to exactly 2^31.  The
+// counter's low 31 bits are zero between barriers, so its top bit flips when, and
+// only when, the last CTA arrives (before that, CTA 0's share borrows from it);
+// a waiting CTA spins until the top bit differs from the one its own arrival saw.
+// The counter needs no reset and the host keeps no state, so the launch can be
+// replayed from a CUDA graph.  Returns false when the wait ran out (~1 s), after
+// setting the timeout bit (oomb_check then clears the whole control block).
 __device__ bool grid_sync(const SelParams& p, int i, bool wait) {
   __shared__ int s_ok;
   __syncthreads();
   if (threadIdx.x == 0) {
     uint32_t* cnt = p.ctrl + kCtrlCount + i;
-    red_release_add(cnt, 1u);
+    const uint32_t add = blockIdx.x == 0 ? 0x80000000u - (gridDim.x - 1u) : 1u;
+    const uint32_t sense = atom_release_add(cnt, add) & 0x80000000u;
     int ok = 1;
     if (wait) {
-      const uint32_t target = p.bar_base[i] + gridDim.x;
       const long long t0 = clock64();
-      while ((int)(ld_acquire(cnt) - target) < 0) {
+      while ((ld_acquire(cnt) & 0x80000000u) == sense) {
         if (clock64() - t0 > kSpinLimit) {
           atomicOr(p.err, OOMB_DEVERR_TIMEOUT);
           ok = 0;
@@ -683,8 +690,7 @@ size_t select_workspace_bytes(const Geometry& g, int n_q) {
 
 cudaError_t launch_page_select(const Geometry& g, const float* summary, const int32_t* table, const void* q,
                                int64_t q_start, int n_q, int top_k, int n_sink, int32_t* sel, int32_t* sel_count,
-                               int max_sel, void* ws, uint32_t* err, uint32_t* ctrl, uint32_t* bar_ctr,
-                               cudaStream_t st) {
+                               int max_sel, void* ws, uint32_t* err, uint32_t* ctrl, cudaStream_t st) {
   const size_t HD = (size_t)g.Hkv * g.d;
   char* w = (char*)ws;
   SelParams p;
@@ -712,7 +718,6 @@ cudaError_t launch_page_select(const Geometry& g, const float* summary, const in
   p.sel_count = sel_count;
   p.err = err;
   p.ctrl = ctrl;
-  for (int i = 0; i < kBarriers; ++i) p.bar_base[i] = bar_ctr[i];
   p.inv_count = 1.0f / ((float)n_q * g.G);
   p.need_scores = p.n_cand > 0 && top_k > 0 && p.n_cand > top_k;
   p.keys_in_smem = p.n_cand <= kMaxSmemKeys;
@@ -751,15 +756,11 @@ cudaError_t launch_page_select(const Geometry& g, const float* summary, const in
     cudaError_t e = set_smem_limit(fn, smem, smem_set[bf16]);
     if (e != cudaSuccess) return e;
   }
-  int per_sm = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, smem);
-  if (e != cudaSuccess) return e;
-  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  // one CTA per SM always fits (<= 200 KB of shared memory, 512 threads); a grid that
+  // could not be co-resident is refused by the cooperative launch itself
   void* args[] = {&p};
-  e = cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(kThreads), args, smem, st);
+  cudaError_t e = cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(kThreads), args, smem, st);
   count_launches(1);
-  if (e == cudaSuccess)
-    for (int i = 0; i < kBarriers; ++i) bar_ctr[i] += (uint32_t)grid;
   return e;
 }
 

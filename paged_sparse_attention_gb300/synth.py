@@ -42,6 +42,7 @@ class Workload:
     plant_beta: float = 1.0
     base_seed: int = 1000
     offload: bool = False
+    window: int = -1      # >= 0: local sliding-window selection of this many history pages (no top-K)
 
     @property
     def group(self) -> int:
@@ -62,6 +63,8 @@ class Workload:
     @property
     def max_sel(self) -> int:
         own = -(-self.chunk // self.page)
+        if self.window >= 0:
+            return min(self.n_pages, self.n_sink + self.window + own)
         if self.top_k < 0:
             return self.n_pages
         return self.n_sink + self.top_k + own
@@ -90,6 +93,11 @@ WORKLOADS: Dict[str, Workload] = {
     # 4M tokens, KV pages in pinned host memory, selected pages prefetched to HBM.
     "offload4m": Workload("offload4m", 28, 4, 128, "bf16", 4194304, 8192, 128, 128,
                           rope=True, plants=8, base_seed=1004, offload=True),
+    # 128K tokens with local sliding-window attention (the sparse layers of a
+    # sparse-native model): the 32 pages (4K tokens) before each 4K chunk plus the
+    # chunk's own pages, no sink and no top-K.
+    "window128k": Workload("window128k", 28, 4, 128, "bf16", 131072, 4096, 128, -1, n_sink=0,
+                           rope=True, base_seed=1005, window=32),
 }
 
 

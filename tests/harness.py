@@ -28,7 +28,8 @@ def make_chunks(w: synth.Workload, plants: bool = True):
 def oracle_sweep(w: synth.Workload, chunks, order, scale: Optional[float] = None):
     scale = 1.0 / math.sqrt(w.head_dim) if scale is None else scale
     return O.chunked_sweep([{k: v.double().numpy() for k, v in ch.items()} for ch in chunks], list(order),
-                           w.n_kv_heads, w.page, len(order), scale, w.top_k, w.n_sink)
+                           w.n_kv_heads, w.page, len(order), scale, w.top_k, w.n_sink,
+                           window=w.window if w.window >= 0 else None)
 
 
 def pad_sel(sel_list: List[np.ndarray], max_sel: int, dev):
@@ -84,7 +85,10 @@ class GpuSweep:
             L.oomb_kv_append(h, g["k"], g["v"], start)
             sel = torch.full((w.n_kv_heads, max_sel), -1, dtype=torch.int32, device=self.dev)
             cnt = torch.zeros(w.n_kv_heads, dtype=torch.int32, device=self.dev)
-            L.oomb_page_select(h, g["q"], start, w.top_k, w.n_sink, sel, cnt, ws_sel)
+            if w.window >= 0:
+                L.oomb_window_select(h, start, n, w.window, w.n_sink, sel, cnt)
+            else:
+                L.oomb_page_select(h, g["q"], start, w.top_k, w.n_sink, sel, cnt, ws_sel)
             self.gpu_sel.append([sel[i, : int(cnt[i])].cpu().numpy() for i in range(w.n_kv_heads)])
             if sel_override is not None:
                 sel, cnt = pad_sel(sel_override[c], max_sel, self.dev)

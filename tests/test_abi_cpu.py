@@ -70,6 +70,9 @@ def test_allocator_host_logic(lib):
     # chunk-level calls before the chunk's K/V exist
     assert lib.oomb_chunk_attn_fwd(pool, fake, 0, 128, fake, fake, 8, 0.1, fake, fake, None) == 1
     assert lib.oomb_page_select(pool, fake, 0, 128, 4, 1, fake, fake, 8, fake, 1 << 30, None) == 1
+    assert lib.oomb_window_select(pool, 0, 128, 2, 1, fake, fake, 8, None) == 1  # chunk not appended
+    assert lib.oomb_window_select(pool, 0, 128, -1, 1, fake, fake, 8, None) == 1  # negative window
+    assert lib.oomb_window_select(pool, 64, 128, 2, 1, fake, fake, 8, None) == 3  # start not on a page
     assert lib.oomb_prefetch(pool, fake, fake, 8, 0, None) == 8  # not an offload pool
     assert lib.oomb_pool_set_stage(pool, 0) == 8
     assert lib.oomb_workspace_size(pool, 0, 4096) > 0

@@ -281,3 +281,69 @@ def test_select_exact_ties(pattern):
         assert np.array_equal(got, np.asarray(ref[h])), (h, got[:8], ref[h][:8])
     assert L.oomb_check(pool.handle) == 0
     pool.close()
+
+
+# -- local sliding-window selection ------------------------------------------------
+WINDOW_CASES = {
+    # Qwen geometry bf16: 3-page window and one sink page, ragged last chunk
+    "bf16_window": synth.scaled(QWEN, "bf16_window", seq=3000, chunk=512, top_k=-1, plants=0, window=3,
+                                n_sink=1),
+    # fp32 tiny geometry: chunk-local attention (no window, no sink)
+    "fp32_local": synth.scaled(synth.WORKLOADS["tiny"], "fp32_local", seq=1000, chunk=256, window=0, n_sink=0),
+    # fp32 GQA 4:2, odd page size, window 2 and two sinks
+    "fp32_window": synth.scaled(synth.WORKLOADS["tiny"], "fp32_window", n_q_heads=4, n_kv_heads=2, head_dim=32,
+                                seq=1111, chunk=240, page=48, window=2, n_sink=2),
+}
+
+
+@pytest.mark.parametrize("name", list(WINDOW_CASES))
+def test_window_sweep_parity(name):
+    """The whole sweep on the GPU's own window selection against the oracle's."""
+    w = WINDOW_CASES[name]
+    chunks, _ = make_chunks(w)
+    order = synth.page_order(w).tolist()
+    ref = oracle_sweep(w, chunks, order)
+    run = GpuSweep(w, chunks, order)
+    assert run.err_bits == 0
+    tol = TOL[w.dtype]
+    for c in range(w.n_chunks):
+        for h in range(w.n_kv_heads):  # integer output: bit-exact
+            assert run.gpu_sel[c][h].tolist() == ref["sel"][c][h].tolist(), (c, h)
+        assert O.rel_l2(f64(run.O[c]), ref["O"][c]) < tol, ("O", c)
+        assert O.rel_l2(f64(run.LSE[c]), ref["LSE"][c]) < tol, ("LSE", c)
+        assert O.rel_l2(f64(run.dQ[c]), ref["dQ"][c]) < tol, ("dQ", c)
+    rdk, rdv = ref["pool"].logical_grads()
+    assert O.rel_l2(f64(run.dK), rdk) < tol
+    assert O.rel_l2(f64(run.dV), rdv) < tol
+    run.pool.close()
+
+
+def test_window_select_edge_cases():
+    """Bit-exact window sets: first chunk, ragged chunk, window longer than the
+    history, sinks beyond the history, window 0; max_sel exactly the set size
+    passes and one less is refused before any device work."""
+    w = synth.scaled(QWEN, "wedge", seq=128 * 12, chunk=128 * 3, top_k=-1, plants=0)
+    chunks, _ = make_chunks(w)
+    dev = torch.device("cuda")
+    pool = PagedKVPool(w.n_q_heads, w.n_kv_heads, w.head_dim, w.page, w.num_phys, w.n_pages, w.torch_dtype,
+                       dev, page_order=synth.page_order(w))
+    for c, ch in enumerate(chunks):
+        L.oomb_kv_append(pool.handle, ch["k"].to(dev), ch["v"].to(dev), w.chunk_bounds(c)[0])
+    for q_start, n_q, window, n_sink in [(0, 384, 3, 1), (384, 384, 0, 0), (768, 384, 1, 1), (1152, 200, 2, 3),
+                                         (1152, 384, 100, 1), (384, 128, 5, 9), (1152, 1, 0, 2)]:
+        ref = O.window_pages(q_start, n_q, w.page, window, n_sink)
+        for max_sel in (len(ref), len(ref) + 5):
+            sel = torch.full((w.n_kv_heads, max_sel), -7, dtype=torch.int32, device=dev)
+            cnt = torch.zeros(w.n_kv_heads, dtype=torch.int32, device=dev)
+            L.oomb_window_select(pool.handle, q_start, n_q, window, n_sink, sel, cnt)
+            torch.cuda.synchronize()
+            for h in range(w.n_kv_heads):
+                assert int(cnt[h]) == len(ref)
+                assert sel[h, : len(ref)].cpu().tolist() == ref.tolist(), (q_start, n_q, window, n_sink, h)
+                assert (sel[h, len(ref):].cpu() == -7).all()  # entries past the count untouched
+        if len(ref) > 1:
+            small = torch.zeros((w.n_kv_heads, len(ref) - 1), dtype=torch.int32, device=dev)
+            with pytest.raises(L.OombError):
+                L.oomb_window_select(pool.handle, q_start, n_q, window, n_sink, small, cnt)
+    assert L.oomb_check(pool.handle) == 0
+    pool.close()
