@@ -6,10 +6,14 @@
 //
 // Kernels of one backward call:
 //   bwd_prep     D_i = dO_i . O_i (fp32) and zero the fp32 dQ accumulator
-//   bwd_main     one CTA per (selected page, KV head): K and V of the page stay in
-//                shared memory; the CTA walks every 128-row query tile that can see
-//                the page, for each of the G query heads of the group, in two
-//                64-row halves:
+//   bwd_main     n_split CTAs per (selected page, KV head), launched page-major
+//                (all KV heads of a page, then the next page; the chunk's own pages,
+//                which see fewer query tiles, last): K and V of the page stay in
+//                shared memory; the page's steps (every 128-row query tile that can
+//                see the page, for each of the G query heads of the group) are cut
+//                into n_split contiguous ranges, one per CTA, chosen on the host
+//                from a model of how the CTAs fill the SMs.  A CTA walks its steps
+//                in two 64-row halves:
 //                  S^T  = K Q_h^T       dP^T = V dO_h^T          (TMEM, fp32)
 //                  P^T  = exp2(S^T scale log2e - LSE log2e)     (masked on the diagonal)
 //                  dS^T = P^T (dP^T - D)
@@ -17,9 +21,9 @@
 //                  dQ^T = K^T dS^T      (dS^T also written to shared memory as the B
 //                                        operand; dQ^T read out of TMEM and added
 //                                        to the fp32 accumulator with global reductions)
-//                and finally adds scale*dK and dV into the block's own rows of the
-//                fp32 gradient pool: no two CTAs own the same rows, so dK/dV need no
-//                atomics.
+//                and finally adds scale*dK and dV into the page's rows of the fp32
+//                gradient pool with 16-byte float reductions (the n_split CTAs of a
+//                page share the rows; a sole owner reads, adds and writes).
 //   bwd_convert  dq = bf16(scale * dQ accumulator), token-major.
 //
 // Warp roles of bwd_main (448 threads):
@@ -31,6 +35,12 @@
 // TMEM columns: half a [0,128), half b [128,256): S^T [0,64) dP^T [64,128); after the
 // softmax, query columns [32c, 32c+32) hold P^T packed in [32c, 32c+16) and dS^T
 // packed in [32c+16, 32c+32), and dQ^T overwrites [64,128); dV [256,384); dK [384,512).
+#include <array>
+#include <map>
+#include <mutex>
+#include <queue>
+#include <vector>
+
 #include "tc_common.cuh"
 
 namespace oomb {
@@ -56,6 +66,7 @@ struct BwdParams {
   float* dv_pool;
   uint32_t* err;
   int max_sel, n_q, n_pad, Hq, G, Hkv, num_phys, max_logical, n_tiles;
+  int n_split;  // CTAs sharing one (page, KV head): each takes a contiguous range of its steps
   int64_t q_start;
   float scale, scale_log2;
   int staged, stage_h0, stage_stride;
@@ -87,7 +98,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
                        const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                        const BwdParams p) {
-  const int s = blockIdx.x, h = blockIdx.y;
+  // page-major order: every KV head of selected page s (and each of its n_split
+  // parts) before page s + 1, so that the lighter own pages run last
+  const int h = (int)(blockIdx.x % (unsigned)p.Hkv);
+  const int r = (int)(blockIdx.x / (unsigned)p.Hkv);
+  const int part = r % p.n_split, s = r / p.n_split;
   if (s >= p.sel_count[h]) return;
   const int first_own = (int)(p.q_start / kTile);
   const int nvis = (int)((p.q_start + p.n_q + kTile - 1) / kTile);
@@ -103,7 +118,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const int own = pg - first_own;           // >= 0 for the chunk's own pages
   const int t0 = own > 0 ? own : 0;
-  const int n_steps = (p.n_tiles - t0) * p.G;
+  // steps (query tile t0 + su / G, query head su % G) for su in [u0, u0 + n_steps)
+  const int all_steps = (p.n_tiles - t0) * p.G;
+  const int u0 = (int)((int64_t)all_steps * part / p.n_split);
+  const int n_steps = (int)((int64_t)all_steps * (part + 1) / p.n_split) - u0;
   if (n_steps <= 0) return;
 
   extern __shared__ uint8_t smem_raw[];
@@ -156,8 +174,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (; v < 2 * n_steps; ++v) {
         const int slot = v % kRing;
         if (v >= kRing && !mbar_wait(&bar->hs_empty[slot], ((v / kRing) - 1) & 1, p.err, abort)) break;
-        const int u = v >> 1, hh = v & 1;
-        const int t = t0 + u / p.G, g = u % p.G;
+        const int su = u0 + (v >> 1), hh = v & 1;
+        const int t = t0 + su / p.G, g = su % p.G;
         const int hq = h * p.G + g;
         const int q0 = t * kTile + hh * kHalf;
         uint8_t* dst = sm + kOffRing + slot * 2 * kHalfTile;
@@ -246,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = tmem_lane_base(warp);
     bool ok = true;
     for (int u = 0; ok && u < n_steps; ++u) {
-      const int t = t0 + u / p.G;
+      const int t = t0 + (u0 + u) / p.G;
       const bool diag = (own >= 0) && (t == own);
       for (int hh = 0; hh < 2; ++hh) {
         const int v = 2 * u + hh, slot = v % kRing;
@@ -312,20 +330,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tmem + lane_off + 256 + 64 * hc + cc * 32, a);
         tmem_ld32(tmem + lane_off + 384 + 64 * hc + cc * 32, b);
         tmem_wait_ld();
+        if (p.n_split > 1) {  // several CTAs add into these rows: 16-byte reductions
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          float4 x = gdv[cc * 8 + e];
-          x.x += __uint_as_float(a[4 * e]);
-          x.y += __uint_as_float(a[4 * e + 1]);
-          x.z += __uint_as_float(a[4 * e + 2]);
-          x.w += __uint_as_float(a[4 * e + 3]);
-          gdv[cc * 8 + e] = x;
-          float4 y = gdk[cc * 8 + e];
-          y.x += p.scale * __uint_as_float(b[4 * e]);
-          y.y += p.scale * __uint_as_float(b[4 * e + 1]);
-          y.z += p.scale * __uint_as_float(b[4 * e + 2]);
-          y.w += p.scale * __uint_as_float(b[4 * e + 3]);
-          gdk[cc * 8 + e] = y;
+          for (int e = 0; e < 8; ++e) {
+            atomicAdd(gdv + cc * 8 + e, make_float4(__uint_as_float(a[4 * e]), __uint_as_float(a[4 * e + 1]),
+                                                    __uint_as_float(a[4 * e + 2]), __uint_as_float(a[4 * e + 3])));
+            atomicAdd(gdk + cc * 8 + e,
+                      make_float4(p.scale * __uint_as_float(b[4 * e]), p.scale * __uint_as_float(b[4 * e + 1]),
+                                  p.scale * __uint_as_float(b[4 * e + 2]), p.scale * __uint_as_float(b[4 * e + 3])));
+          }
+        } else {  // sole owner of the rows: read, add, write
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            float4 x = gdv[cc * 8 + e];
+            x.x += __uint_as_float(a[4 * e]);
+            x.y += __uint_as_float(a[4 * e + 1]);
+            x.z += __uint_as_float(a[4 * e + 2]);
+            x.w += __uint_as_float(a[4 * e + 3]);
+            gdv[cc * 8 + e] = x;
+            float4 y = gdk[cc * 8 + e];
+            y.x += p.scale * __uint_as_float(b[4 * e]);
+            y.y += p.scale * __uint_as_float(b[4 * e + 1]);
+            y.z += p.scale * __uint_as_float(b[4 * e + 2]);
+            y.w += p.scale * __uint_as_float(b[4 * e + 3]);
+            gdk[cc * 8 + e] = y;
+          }
         }
       }
     }
@@ -338,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = tmem_lane_base(warp);
     bool ok = true;
     for (int u = 0; ok && u < n_steps; ++u) {
-      const int t = t0 + u / p.G, g = u % p.G;
+      const int t = t0 + (u0 + u) / p.G, g = (u0 + u) % p.G;
       const int hq = h * p.G + g;
       for (int hh = 0; hh < 2; ++hh) {
         uint32_t r[64];
@@ -419,6 +448,63 @@ __global__ void bwd_convert(const float* __restrict__ dq_acc, int n_q, int Hq, f
 
 }  // namespace
 
+// How many CTAs share one (page, KV head).  A CTA's work is its number of steps
+// (query tile x query head); history pages have n_tiles * G of them and the chunk's
+// own page k has (n_tiles - k) * G.  With one CTA per SM, CTAs start in launch order
+// on the first SM that frees up; that greedy schedule is replayed here for
+// kMinSplit..kMaxSplit parts, each CTA also paying a fixed cost (K/V load, pipeline
+// fill and drain, the dK/dV epilogue) of about one step, and the fewest parts within
+// 1% of the shortest schedule win.  Measured on GB300 (backward calls of whole
+// sweeps), two parts beat one on every workload, also where this model sees no
+// tail (1M tokens, chunks of 8192: 923 against 906 TFLOP/s), so two is the floor;
+// three win where the grid is small (a 4K-token window over 4K chunks: 857 against
+// 838 with two, 671 with one).  The selection counts live on the device, so every
+// one of the max_sel slots is assumed filled; empty slots exit at once.  Cached per
+// shape.
+constexpr int kMinSplit = 2;
+constexpr int kMaxSplit = 4;
+constexpr double kCtaOverheadSteps = 1.0;
+
+int bwd_split(int max_sel, int n_own, int n_tiles, int G, int Hkv, int n_sm) {
+  static std::mutex mu;
+  static std::map<std::array<int, 6>, int> cache;
+  const std::array<int, 6> key = {max_sel, n_own, n_tiles, G, Hkv, n_sm};
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  const int n_hist = std::max(0, max_sel - n_own);
+  int best = kMinSplit;
+  double best_t = 0.0;
+  for (int ns = kMinSplit; ns <= kMaxSplit; ++ns) {
+    std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
+    for (int i = 0; i < n_sm; ++i) free_at.push(0.0);
+    double end = 0.0;
+    for (int sl = 0; sl < max_sel; ++sl) {
+      const int k = sl - n_hist;  // own page index (< 0: history page)
+      const int steps = (n_tiles - (k > 0 ? k : 0)) * G;
+      for (int part = 0; part < ns; ++part) {
+        const int w = (int)((int64_t)steps * (part + 1) / ns - (int64_t)steps * part / ns);
+        if (w <= 0) continue;
+        for (int hk = 0; hk < Hkv; ++hk) {
+          const double t = free_at.top() + kCtaOverheadSteps + w;
+          free_at.pop();
+          free_at.push(t);
+          end = std::max(end, t);
+        }
+      }
+    }
+    if (ns == kMinSplit || end < 0.99 * best_t) {
+      best = ns;
+      best_t = end;
+    }
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  cache[key] = best;
+  return best;
+}
+
 size_t bwd_tc_workspace_bytes(const Geometry& g, int n_q) {
   const size_t n_pad = (size_t)(n_q + kTile - 1) / kTile * kTile;
   return 2 * align_up((size_t)g.Hq * n_pad * 4, 256) + align_up((size_t)g.Hq * n_q * kD * 4, 256);
@@ -467,7 +553,10 @@ cudaError_t launch_attn_bwd_tc(const AttnArgs& a, cudaStream_t st) {
   p.staged = a.kv.staged;
   p.stage_h0 = a.kv.stage_h0;
   p.stage_stride = a.kv.stage_stride;
-  dim3 grid(a.max_sel, a.g.Hkv);
+  const int first_own = (int)(a.q_start / kTile);
+  const int n_own = (int)((a.q_start + a.n_q + kTile - 1) / kTile) - first_own;
+  p.n_split = bwd_split(a.max_sel, n_own, p.n_tiles, p.G, p.Hkv, device_sm_count());
+  const unsigned grid = (unsigned)a.max_sel * (unsigned)p.n_split * (unsigned)p.Hkv;
   attn_bwd_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(tq, tdo, tk, tv, p);
   bwd_convert<<<(warps + 7) / 8, 256, 0, st>>>(dq_acc, a.n_q, a.g.Hq, a.scale,
                                                reinterpret_cast<__nv_bfloat16*>(a.dq));

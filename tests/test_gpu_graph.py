@@ -1,7 +1,7 @@
 """A whole step captured in one CUDA graph and replayed gives the eager step's
 results: the same selections (bit-exact; the selection's grid barriers keep no
-host state, so replays reuse the captured launch), and the same O-dependent
-outputs dQ, dK, dV up to the order of the fp32 dQ reductions.  Also checked
+host state, so replays reuse the captured launch), and the same dQ, dK, dV up to
+the order of their fp32 reductions across thread blocks.  Also checked
 against the oracle on the window workload's last chunk."""
 import math
 import os
@@ -63,9 +63,15 @@ def test_graph_replay_matches_eager(kind):
         g.replay()
     torch.cuda.synchronize()
     assert L.oomb_check(step.pool.handle) == 0
-    assert torch.equal(step.sel, sel0) and torch.equal(step.cnt, cnt0)
+    assert torch.equal(step.cnt, cnt0)
+    for c in range(w.n_chunks):  # entries past a count are not written by a selection
+        for h in range(w.n_kv_heads):
+            k = int(cnt0[c, h])
+            assert torch.equal(step.sel[c, h, :k], sel0[c, h, :k]), (c, h)
+    # fp32 sums reduced across thread blocks in a run-dependent order: equal to rounding
+    # (dQ is then rounded to bf16, where such differences can flip the last bit)
     for d, d0 in zip(step.dq, dq0):
-        assert O.rel_l2(f64(d), f64(d0)) < 1e-6
+        assert O.rel_l2(f64(d), f64(d0)) < 1e-4
     assert O.rel_l2(f64(step.pool.dk_pool), f64(dk0)) < 1e-6
     assert O.rel_l2(f64(step.pool.dv_pool), f64(dv0)) < 1e-6
 

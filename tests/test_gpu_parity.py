@@ -186,8 +186,9 @@ def test_host_errors_on_gpu():
 @pytest.mark.parametrize("name", ["bf16_sparse", "fp32_sparse"])
 def test_offload_matches_resident(name):
     """K/V pools in pinned host memory, selected pages prefetched on a side stream:
-    same outputs as the HBM-resident run (bitwise for O, LSE, dK, dV; dQ is summed
-    across thread blocks in a run-dependent order), and within tolerance of the oracle."""
+    same outputs as the HBM-resident run (bitwise for O and LSE; dQ, and dK/dV of
+    pages whose backward is split over several thread blocks, are summed with float
+    reductions in a run-dependent order), and within tolerance of the oracle."""
     w = CASES[name]
     chunks, _ = make_chunks(w)
     order = synth.page_order(w).tolist()
@@ -199,7 +200,7 @@ def test_offload_matches_resident(name):
         assert torch.equal(off.O[c], res.O[c]) and torch.equal(off.LSE[c], res.LSE[c])
         assert O.rel_l2(f64(off.dQ[c]), f64(res.dQ[c])) < 1e-3
         assert O.rel_l2(f64(off.dQ[c]), ref["dQ"][c]) < TOL[w.dtype]
-    assert torch.equal(off.dK, res.dK) and torch.equal(off.dV, res.dV)
+    assert O.rel_l2(f64(off.dK), f64(res.dK)) < 1e-6 and O.rel_l2(f64(off.dV), f64(res.dV)) < 1e-6
     for a, b in zip(off.gpu_sel, res.gpu_sel):
         for x, y in zip(a, b):
             assert np.array_equal(x, y)
