@@ -589,6 +589,12 @@ def main():
     launches = L.oomb_launch_count() - launches0
     ms = reduce_max_ms(e0.elapsed_time(e1) / args.steps, world, dev)
     L.oomb_check(step.pool.handle)
+    # end to end right after the device-resident steps, before the other variants
+    e2e = None
+    if not args.no_e2e:
+        with ClockSampler(local) as clk_e2e:
+            e2e = measure_e2e(step, args.steps, credited, world, dev)
+        e2e["clocks"] = clk_e2e.summary()
 
     # per-kernel-call roofline: the backward (dominant) and forward calls
     bwd_ms = [a.elapsed_time(b) for a, b, _ in step.bwd_events]
@@ -713,8 +719,8 @@ def main():
             "gpu_launches": int(launches),
             "clocks": clk.summary()}
 
-    if not args.no_e2e:
-        line["e2e"] = measure_e2e(step, args.steps, credited, world, dev)
+    if e2e is not None:
+        line["e2e"] = e2e
     if rank == 0 and not args.no_cpu_baseline and world == 1:
         cb = oracle_sample_seconds(w, budget_s=15.0)
         line["cpu_baseline"] = {"value": cb["flops"] / cb["seconds"] / 1e12, "unit": UNIT, "cores": cb["cores"],

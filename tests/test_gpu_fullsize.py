@@ -180,3 +180,54 @@ def test_sparse1m_last_chunk_fullsize():
         assert O.rel_l2(f64(o[r0:r0 + 128, :G]), Oo) < 1e-2, r0
         assert O.rel_l2(f64(lse[:G, r0:r0 + 128]), Lo) < 1e-2, r0
     step.pool.close()
+
+
+def test_window128k_fullsize():
+    """128K tokens, local window of 32 pages before each 4K chunk (no sink), as
+    bench.Step runs it: every chunk's selection for every KV head bit-exact against
+    the oracle's window set, then KV group 0 of the last chunk against the oracle:
+    the forward for its first and last 128 rows and dQ for its last 128 rows."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_sparse_attention_gb300 import build
+    build.build()
+    w = synth.WORKLOADS["window128k"]
+    dev = torch.device("cuda")
+    step = bench.Step(w, dev)
+    step.run()
+    torch.cuda.synchronize()
+    assert L.oomb_check(step.pool.handle) == 0
+    S, G = w.n_chunks, w.group
+    sel_all, cnt_all = step.sel.cpu().numpy(), step.cnt.cpu().numpy()
+    for c in range(S):
+        start, n = w.chunk_bounds(c)
+        ref = O.window_pages(start, n, w.page, w.window, w.n_sink)
+        for h in range(w.n_kv_heads):
+            assert sel_all[c, h, : cnt_all[c, h]].tolist() == ref.tolist(), (c, h)
+    order = synth.page_order(w).tolist()
+    pool = O.OraclePool(1, w.head_dim, w.page, w.num_phys, w.n_pages)
+    used = 0
+    for c in range(S):
+        start, n = w.chunk_bounds(c)
+        ch = step.chunks[c]
+        npg = -(-n // w.page)
+        pool.append(ch["k"][:, 0:1].double().cpu().numpy(), ch["v"][:, 0:1].double().cpu().numpy(), start,
+                    order[used:used + npg])
+        used += npg
+    c = S - 1
+    start, n = w.chunk_bounds(c)
+    sel = [O.window_pages(start, n, w.page, w.window, w.n_sink)]
+    q = step.chunks[c]["q"][:, :G].double().cpu().numpy()
+    do = step.chunks[c]["do"][:, :G].double().cpu().numpy()
+    scale = 1.0 / math.sqrt(w.head_dim)
+    step._fwd(c, step.chunks[c], start, n, False)  # O, LSE of chunk c (no side effects)
+    torch.cuda.synchronize()
+    for r0 in (0, n - 128):
+        Oo, Lo = O.chunk_attn_fwd(pool, q[r0:r0 + 128], start + r0, sel, scale)
+        assert O.rel_l2(f64(step.o[r0:r0 + 128, :G]), Oo) < 1e-2, r0
+        assert O.rel_l2(f64(step.lse[:G, r0:r0 + 128]), Lo) < 1e-2, r0
+    r0 = n - 128
+    Oo, Lo = O.chunk_attn_fwd(pool, q[r0:], start + r0, sel, scale)
+    dq_ref = O.chunk_attn_bwd(pool, q[r0:], Oo, do[r0:], Lo, start + r0, sel, scale)
+    assert O.rel_l2(f64(step.dq[c][r0:, :G]), dq_ref) < 1e-2
+    step.pool.close()

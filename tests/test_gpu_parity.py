@@ -37,6 +37,19 @@ CASES = {
 }
 
 
+# -- local sliding-window selection ------------------------------------------------
+WINDOW_CASES = {
+    # Qwen geometry bf16: 3-page window and one sink page, ragged last chunk
+    "bf16_window": synth.scaled(QWEN, "bf16_window", seq=3000, chunk=512, top_k=-1, plants=0, window=3,
+                                n_sink=1),
+    # fp32 tiny geometry: chunk-local attention (no window, no sink)
+    "fp32_local": synth.scaled(synth.WORKLOADS["tiny"], "fp32_local", seq=1000, chunk=256, window=0, n_sink=0),
+    # fp32 GQA 4:2, odd page size, window 2 and two sinks
+    "fp32_window": synth.scaled(synth.WORKLOADS["tiny"], "fp32_window", n_q_heads=4, n_kv_heads=2, head_dim=32,
+                                seq=1111, chunk=240, page=48, window=2, n_sink=2),
+}
+
+
 @pytest.fixture(scope="module", autouse=True)
 def _built():
     from paged_sparse_attention_gb300 import build
@@ -183,13 +196,13 @@ def test_host_errors_on_gpu():
     pool.close()
 
 
-@pytest.mark.parametrize("name", ["bf16_sparse", "fp32_sparse"])
+@pytest.mark.parametrize("name", ["bf16_sparse", "fp32_sparse", "bf16_window"])
 def test_offload_matches_resident(name):
     """K/V pools in pinned host memory, selected pages prefetched on a side stream:
     same outputs as the HBM-resident run (bitwise for O and LSE; dQ, and dK/dV of
     pages whose backward is split over several thread blocks, are summed with float
     reductions in a run-dependent order), and within tolerance of the oracle."""
-    w = CASES[name]
+    w = {**CASES, **WINDOW_CASES}[name]
     chunks, _ = make_chunks(w)
     order = synth.page_order(w).tolist()
     ref = oracle_sweep(w, chunks, order)
@@ -282,19 +295,6 @@ def test_select_exact_ties(pattern):
         assert np.array_equal(got, np.asarray(ref[h])), (h, got[:8], ref[h][:8])
     assert L.oomb_check(pool.handle) == 0
     pool.close()
-
-
-# -- local sliding-window selection ------------------------------------------------
-WINDOW_CASES = {
-    # Qwen geometry bf16: 3-page window and one sink page, ragged last chunk
-    "bf16_window": synth.scaled(QWEN, "bf16_window", seq=3000, chunk=512, top_k=-1, plants=0, window=3,
-                                n_sink=1),
-    # fp32 tiny geometry: chunk-local attention (no window, no sink)
-    "fp32_local": synth.scaled(synth.WORKLOADS["tiny"], "fp32_local", seq=1000, chunk=256, window=0, n_sink=0),
-    # fp32 GQA 4:2, odd page size, window 2 and two sinks
-    "fp32_window": synth.scaled(synth.WORKLOADS["tiny"], "fp32_window", n_q_heads=4, n_kv_heads=2, head_dim=32,
-                                seq=1111, chunk=240, page=48, window=2, n_sink=2),
-}
 
 
 @pytest.mark.parametrize("name", list(WINDOW_CASES))
