@@ -225,8 +225,12 @@ OOMB_API oomb_status oomb_chunk_attn_fwd(oomb_pool* pool, const void* q, int64_t
  *   dq = scale dS K (written, dtype),
  *   dK_pool[phi(p), h] += scale dS^T Q,  dV_pool[phi(p), h] += P^T dO
  * summed over the G query heads of KV head h and every row of the chunk.
- * Each (page, KV head) block of the gradient pool is updated by exactly one
- * thread block: no global atomics on dK/dV.
+ * Summation order: on the tensor-core path (bf16, head_dim = page = 128) the
+ * work of each (page, KV head) block is split over 2-4 thread blocks that add
+ * their partial dK/dV with float reductions, and dq is accumulated in fp32 across
+ * thread blocks, so repeated runs agree to rounding, not bit for bit; the SIMT
+ * path (other shapes, fp32) gives each gradient row one owner and is
+ * deterministic.  Backward calls on one pool must be stream-ordered.
  * Workspace: oomb_workspace_size(OOMB_OP_BWD, n_q) bytes, contents scratch.
  * Errors: ARG, ALIGN, WORKSPACE, UNSUPPORTED, CUDA. */
 OOMB_API oomb_status oomb_chunk_attn_bwd(oomb_pool* pool, const void* q, const void* o, const void* d_o, const float* lse,
