@@ -641,10 +641,10 @@ def main():
         pf_bytes = {c: int(cnt[c].sum()) * w.page * w.head_dim * 2 * esz for c in range(w.n_chunks)}
         pf_s = sum(a.elapsed_time(b) for a, b, _ in step.prefetch_events) * 1e-3
         pf_b = sum(pf_bytes[c] for _, _, c in step.prefetch_events)
-        # isolated: the gather of the last chunks alone, and a plain pinned-host -> HBM copy
-        # isolated: each of the last chunks' gathers three times in a row; the first
-        # gather of a page set after the step can take far longer than the repeats
-        # (it is reported on its own), the repeats give the gather's bandwidth
+        # isolated: each of the last chunks' gathers three times in a row (the first
+        # gather of a page set after the step can take far longer than the repeats,
+        # so it is reported on its own; the repeats give the gather's bandwidth), and
+        # a plain pinned-host -> HBM copy for the link's bandwidth
         iso, first_ms = [], []
         for c in range(max(0, w.n_chunks - 3), w.n_chunks):
             for rep in range(3):
