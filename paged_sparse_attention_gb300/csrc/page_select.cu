@@ -30,7 +30,7 @@
 //                    key above it and, among keys equal to it, the lowest pages.
 // Every sum runs in a fixed order and the histogram is integer, so the selection
 // is deterministic.  The barrier counters live in the pool's control block and
-// only grow; the host passes the value each had before the call.
+// are sense-reversing (see grid_sync): the host keeps no state between calls.
 #include "oomb_internal.h"
 #include "sm103_ptx.cuh"
 
