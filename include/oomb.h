@@ -128,6 +128,20 @@ OOMB_API void oomb_pool_destroy(oomb_pool* pool);
  * page-table entry to -1 (stream-ordered).  The pools' contents are kept. */
 OOMB_API oomb_status oomb_pool_reset(oomb_pool* pool, void* stream);
 
+/* Return logical pages [first_logical_page, first_logical_page + n_pages) to the
+ * free list (explainer 2.B: fixed-size pages; "3. Key Contributions": paged
+ * memory without fragmentation).  Every page of the range must be mapped (already
+ * appended and not yet freed).  Their page-table entries become -1 on `stream`
+ * and their physical pages are handed out first by the next appends (lowest
+ * logical page first); the pool's token count is unchanged, so later appends
+ * continue at the end.  A freed page must not be selected again: the attention
+ * kernels and the top-K selection flag an unmapped page (OOMB_DEVERR_PAGE) and
+ * skip it, so free only pages that no later selection reaches (pages behind a
+ * local window, oomb_window_select; a finished sequence).
+ * Errors: ARG (range outside the appended pages, or a page not mapped), CUDA
+ * (nothing changes on the host). */
+OOMB_API oomb_status oomb_page_free(oomb_pool* pool, int64_t first_logical_page, int n_pages, void* stream);
+
 /* Paged KV append (explainer 2.B "Paged KV Cache and Gradient Management"; the
  * lay summary's "Trick A": each chunk's KV drops onto the next free page, no
  * copying of earlier pages).  Opens ceil((first_token+n)/P) - first_token/P new

@@ -77,6 +77,7 @@ def load(path: str = LIB_PATH) -> C.CDLL:
         "oomb_launch_count": (C.c_uint64, []),
         "oomb_page_select_noalloc": (i32, [vp, vp, i64, i32, i32, i32, vp, vp, i32, vp]),
         "oomb_window_select": (i32, [vp, i64, i32, i32, i32, vp, vp, i32, vp]),
+        "oomb_page_free": (i32, [vp, i64, i32, vp]),
         "oomb_last_cuda_error": (C.c_char_p, []),
     }
     for name, (res, args) in sig.items():
@@ -135,6 +136,10 @@ def oomb_page_select(pool: int, q, q_start: int, top_k: int, n_sink: int, sel, s
     _ok("oomb_page_select", load().oomb_page_select(pool, _ptr(q), q_start, n, top_k, n_sink, _ptr(sel),
                                                     _ptr(sel_count), sel.shape[-1], _ptr(workspace), ws_bytes,
                                                     _stream(stream)))
+
+
+def oomb_page_free(pool: int, first_logical_page: int, n_pages: int, stream=None) -> None:
+    _ok("oomb_page_free", load().oomb_page_free(pool, first_logical_page, n_pages, _stream(stream)))
 
 
 def oomb_window_select(pool: int, q_start: int, n_q: int, window: int, n_sink: int, sel, sel_count,

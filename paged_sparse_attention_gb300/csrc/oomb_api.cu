@@ -242,6 +242,24 @@ oomb_status oomb_kv_append(oomb_pool* p, const void* k, const void* v, int64_t f
   return OOMB_OK;
 }
 
+oomb_status oomb_page_free(oomb_pool* p, int64_t first_logical_page, int n_pages, void* stream) {
+  if (!p || first_logical_page < 0 || n_pages <= 0) return OOMB_ERR_ARG;
+  const int P = p->g.P;
+  const int64_t end = first_logical_page + n_pages;
+  if (end > (p->n_tokens + P - 1) / P) return OOMB_ERR_ARG;  // only appended pages
+  for (int64_t i = first_logical_page; i < end; ++i)
+    if (p->table[i] < 0) return OOMB_ERR_ARG;  // freed already
+  cudaError_t e = cudaMemsetAsync(p->d.page_table + first_logical_page, 0xFF, sizeof(int32_t) * (size_t)n_pages,
+                                  (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_status(e);
+  // the free list hands out from its back: push the highest page first
+  for (int64_t i = end - 1; i >= first_logical_page; --i) {
+    p->free_list.push_back(p->table[i]);
+    p->table[i] = -1;
+  }
+  return OOMB_OK;
+}
+
 size_t oomb_workspace_size(const oomb_pool* p, int op, int n_q) {
   if (!p || n_q <= 0) return 0;
   if (op == OOMB_OP_SELECT) return select_workspace_bytes(p->g, n_q);

@@ -71,6 +71,8 @@ def test_allocator_host_logic(lib):
     assert lib.oomb_chunk_attn_fwd(pool, fake, 0, 128, fake, fake, 8, 0.1, fake, fake, None) == 1
     assert lib.oomb_page_select(pool, fake, 0, 128, 4, 1, fake, fake, 8, fake, 1 << 30, None) == 1
     assert lib.oomb_window_select(pool, 0, 128, 2, 1, fake, fake, 8, None) == 1  # chunk not appended
+    assert lib.oomb_page_free(pool, 0, 1, None) == 1  # nothing appended yet
+    assert lib.oomb_page_free(pool, -1, 1, None) == 1 and lib.oomb_page_free(pool, 0, 0, None) == 1
     assert lib.oomb_window_select(pool, 0, 128, -1, 1, fake, fake, 8, None) == 1  # negative window
     assert lib.oomb_window_select(pool, 64, 128, 2, 1, fake, fake, 8, None) == 3  # start not on a page
     assert lib.oomb_prefetch(pool, fake, fake, 8, 0, None) == 8  # not an offload pool

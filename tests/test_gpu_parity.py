@@ -348,3 +348,49 @@ def test_window_select_edge_cases():
                 L.oomb_window_select(pool.handle, q_start, n_q, window, n_sink, small, cnt)
     assert L.oomb_check(pool.handle) == 0
     pool.close()
+
+
+def test_page_free_and_reuse():
+    """Pages behind a local window are freed: their table entries become -1 (host
+    and device), the window forward is unchanged bit for bit, a second free or a
+    range past the appended pages is refused, and the next append takes the freed
+    physical pages, lowest logical page first, with its K/V copied exactly."""
+    w = synth.scaled(QWEN, "pfree", seq=128 * 12, chunk=128 * 3, top_k=-1, plants=0, window=2, n_sink=1)
+    chunks, _ = make_chunks(w)
+    dev = torch.device("cuda")
+    order = synth.page_order(w)
+    pool = PagedKVPool(w.n_q_heads, w.n_kv_heads, w.head_dim, w.page, w.num_phys, w.n_pages + 3, w.torch_dtype,
+                       dev, page_order=order)
+    for c, ch in enumerate(chunks):
+        L.oomb_kv_append(pool.handle, ch["k"].to(dev), ch["v"].to(dev), w.chunk_bounds(c)[0])
+    c = w.n_chunks - 1
+    start, n = w.chunk_bounds(c)
+    q = chunks[c]["q"].to(dev)
+    sel = torch.full((w.n_kv_heads, 8), -1, dtype=torch.int32, device=dev)
+    cnt = torch.zeros(w.n_kv_heads, dtype=torch.int32, device=dev)
+    L.oomb_window_select(pool.handle, start, n, w.window, w.n_sink, sel, cnt)
+    scale = 1.0 / math.sqrt(w.head_dim)
+    o1, l1 = torch.empty_like(q), torch.empty(w.n_q_heads, n, dtype=torch.float32, device=dev)
+    L.oomb_chunk_attn_fwd(pool.handle, q, start, sel, cnt, scale, o1, l1)
+    before = pool.table_host(w.n_pages)
+    freed = before[1:7]  # logical pages 1..6: behind the window {0, 7, 8} + own {9, 10, 11}
+    L.oomb_page_free(pool.handle, 1, 6)
+    after = pool.table_host(w.n_pages)
+    assert after[1:7] == [-1] * 6 and after[:1] == before[:1] and after[7:] == before[7:]
+    assert pool.page_table[: w.n_pages].cpu().tolist() == after
+    assert L.oomb_pool_free_pages(pool.handle) == w.num_phys - w.n_pages + 6
+    o2, l2 = torch.empty_like(o1), torch.empty_like(l1)
+    L.oomb_chunk_attn_fwd(pool.handle, q, start, sel, cnt, scale, o2, l2)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    for bad in [(3, 1), (11, 2), (12, 1)]:  # freed already; past the appended pages
+        with pytest.raises(L.OombError):
+            L.oomb_page_free(pool.handle, *bad)
+    # the next append (3 pages) reuses the freed physical pages of logical pages 1, 2, 3
+    k, v = chunks[0]["k"].to(dev), chunks[0]["v"].to(dev)
+    L.oomb_kv_append(pool.handle, k, v, w.seq)
+    tab = pool.table_host(w.n_pages + 3)
+    assert tab[w.n_pages:] == freed[:3]
+    kk, vv = pool.logical_kv(w.seq + k.shape[0])
+    assert torch.equal(kk[w.seq:].cpu(), chunks[0]["k"]) and torch.equal(vv[w.seq:].cpu(), chunks[0]["v"])
+    assert L.oomb_check(pool.handle) == 0
+    pool.close()
