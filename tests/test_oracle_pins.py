@@ -352,3 +352,35 @@ def test_window_off_by_one_is_caught(monkeypatch):
     monkeypatch.setattr(O, "window_pages", good)
     Ot, _, _, _ = _sdpa_masked(Q, K, V, dO, 0.5, _window_mask(N, C, P, 2, 1))
     assert O.rel_l2(_cat(res, "O"), Ot) > 1e-3
+
+
+def test_degenerate_cases():
+    """G = 1 is multi-head attention (no repeat needed): the paged sweep equals torch
+    fp64 SDPA on the unrepeated heads; one chunk (C = N) is plain causal attention;
+    a K at least the number of candidates selects everything, so the sweep equals
+    the dense run bit for bit."""
+    rng = np.random.default_rng(21)
+    N, P, H, d = 48, 8, 3, 8
+    Q, K, V, dO = _rand_seq(rng, N, H, H, d)
+    scale = 1.0 / math.sqrt(d)
+    order = rng.permutation(N // P)
+    for C in (16, N):  # several chunks, and a single chunk
+        res = _sweep(Q, K, V, dO, C, P, scale, order)
+        tq = torch.tensor(Q.transpose(1, 0, 2), requires_grad=True)
+        tk = torch.tensor(K.transpose(1, 0, 2), requires_grad=True)
+        tv = torch.tensor(V.transpose(1, 0, 2), requires_grad=True)
+        to = torch.nn.functional.scaled_dot_product_attention(tq[None], tk[None], tv[None], is_causal=True,
+                                                              scale=scale)[0]
+        (to * torch.tensor(dO.transpose(1, 0, 2))).sum().backward()
+        dK, dV = res["pool"].logical_grads()
+        assert O.rel_l2(_cat(res, "O"), to.detach().numpy().transpose(1, 0, 2)) < 1e-12
+        assert O.rel_l2(np.concatenate(res["dQ"]), tq.grad.numpy().transpose(1, 0, 2)) < 1e-12
+        assert O.rel_l2(dK, tk.grad.numpy().transpose(1, 0, 2)) < 1e-12
+        assert O.rel_l2(dV, tv.grad.numpy().transpose(1, 0, 2)) < 1e-12
+    dense = _sweep(Q, K, V, dO, 16, P, scale, order, top_k=-1, n_sink=1)
+    big_k = _sweep(Q, K, V, dO, 16, P, scale, order, top_k=N // P, n_sink=1)
+    for key in ("O", "LSE"):
+        for a, b in zip(dense[key], big_k[key]):
+            assert np.array_equal(a, b)
+    for a, b in zip(dense["sel"], big_k["sel"]):
+        assert all(np.array_equal(x, y) for x, y in zip(a, b))
