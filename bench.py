@@ -512,6 +512,7 @@ def run_reference(args, w, rank, world):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": w.name, "seq": w.seq, "chunk": w.chunk, "page": w.page, "top_k": w.top_k,
+                       **({"window_pages": w.window, "n_sink": w.n_sink} if w.window >= 0 else {}),
                        "heads": f"{w.n_q_heads}/{w.n_kv_heads}", "head_dim": w.head_dim},
             "cpu_baseline": {"value": tflops, "unit": UNIT, "cores": res[0]["cores"], "kind": "oracle",
                              "sample": res[0]["sample"]},
