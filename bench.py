@@ -31,8 +31,12 @@ sys.path.insert(0, ROOT)
 
 METRIC = "paged sparse chunk-attn fwd+bwd TFLOP/s and tokens/s/layer at 1 GB300; % roofline"
 UNIT = "TFLOP/s"
+# used when the machine has no measured-peaks file: GB300 figures measured earlier on
+# this pool (copy 6783 GB/s; bf16 dense GEMM 1875.1 TFLOP/s burst, 1690.3 sustained),
+# close to the published fallback of 6.8 TB/s and 1.9 / 1.7 PFLOP/s
 FALLBACK_PEAKS = {"hbm_gbs": 6783.0, "bf16_tflops": 1875.1, "bf16_tflops_sustained": 1690.3,
-                  "source": "measured GB300 peaks (STREAM-style copy, cuBLAS bf16 GEMM) as recorded for this pool"}
+                  "source": "fallback (no measured-peaks file on this machine): GB300 copy and cuBLAS bf16 "
+                            "figures measured earlier on this pool"}
 
 
 _T0 = time.time()
@@ -49,7 +53,7 @@ def load_peaks():
     if os.path.exists(path):
         with open(path) as f:
             d = json.load(f)
-        d.setdefault("source", "MEASURED_PEAKS.json")
+        d.setdefault("source", "measured (MEASURED_PEAKS.json)")
         return d
     return dict(FALLBACK_PEAKS)
 
