@@ -1,0 +1,74 @@
+"""The benchmark's credited work, checked by brute force on the CPU: the number of
+selected, causally visible (query, key) pairs per chunk (summed over query heads)
+that bench.py multiplies by 14 d FLOPs, for dense, top-K-like and window
+selections, including a ragged last chunk and a partial last page."""
+import os
+import sys
+import types
+
+import numpy as np
+import torch
+
+from paged_sparse_attention_gb300 import synth
+
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+import bench  # noqa: E402
+
+
+def _brute(w, sel, cnt):
+    out = []
+    for c in range(w.n_chunks):
+        start, n = w.chunk_bounds(c)
+        tot = 0
+        for h in range(w.n_kv_heads):
+            keys = [p * w.page + t for p in sel[c, h, : cnt[c, h]] for t in range(w.page)
+                    if p * w.page + t < start + n]
+            for i in range(start, start + n):
+                tot += sum(1 for j in keys if j <= i)
+        out.append(tot * w.group)
+    return out
+
+
+def _count(w, sel, cnt):
+    ns = types.SimpleNamespace(w=w, sel=torch.from_numpy(sel), cnt=torch.from_numpy(cnt))
+    return bench.Step.pairs_per_chunk(ns)
+
+
+def _selections(w, kind, rng):
+    sel = np.full((w.n_chunks, w.n_kv_heads, w.n_pages), -1, dtype=np.int32)
+    cnt = np.zeros((w.n_chunks, w.n_kv_heads), dtype=np.int32)
+    for c in range(w.n_chunks):
+        start, n = w.chunk_bounds(c)
+        n_hist = start // w.page
+        own = list(range(n_hist, (start + n - 1) // w.page + 1))
+        for h in range(w.n_kv_heads):
+            if kind == "dense":
+                pages = list(range(n_hist)) + own
+            elif kind == "window":
+                pages = [int(p) for p in range(max(0, n_hist - 2), n_hist)] + own
+            else:  # a random subset of the history (different per head) plus the own pages
+                k = min(n_hist, 3)
+                pages = sorted(rng.choice(n_hist, size=k, replace=False).tolist()) + own if n_hist else own
+            sel[c, h, : len(pages)] = pages
+            cnt[c, h] = len(pages)
+    return sel, cnt
+
+
+def test_credited_pairs_match_brute_force():
+    rng = np.random.default_rng(3)
+    base = synth.WORKLOADS["tiny"]
+    for kind in ("dense", "topk", "window"):
+        # 4 query heads / 2 KV heads, pages of 8, chunks of 24 with a ragged last chunk of 13
+        w = synth.scaled(base, f"acct_{kind}", n_q_heads=4, n_kv_heads=2, seq=85, chunk=24, page=8)
+        sel, cnt = _selections(w, kind, rng)
+        assert _count(w, sel, cnt) == _brute(w, sel, cnt), kind
+
+
+def test_dense_credit_closed_form():
+    """All pages selected: chunk c credits sum over its rows of (start + i + 1) keys."""
+    w = synth.scaled(synth.WORKLOADS["tiny"], "acct_closed", n_q_heads=6, n_kv_heads=3, seq=100, chunk=32, page=8)
+    sel, cnt = _selections(w, "dense", np.random.default_rng(0))
+    got = _count(w, sel, cnt)
+    for c in range(w.n_chunks):
+        start, n = w.chunk_bounds(c)
+        assert got[c] == sum(start + i + 1 for i in range(n)) * w.n_q_heads
