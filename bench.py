@@ -267,6 +267,14 @@ class Step:
             self._timed(record, self.sel_events, c, L.oomb_page_select, h, ch["q"], start, w.top_k, w.n_sink,
                         self.sel[c], self.cnt[c], self.ws_sel)
 
+    def scored_chunks(self):
+        """Chunks whose selection scores pages (top-K over more candidates than K)."""
+        w = self.w
+        if w.window >= 0 or w.top_k < 0:
+            return set()
+        return {c for c in range(w.n_chunks)
+                if max(0, w.chunk_bounds(c)[0] // w.page - w.n_sink) > w.top_k}
+
     def hbm_bytes(self):
         """Algorithmic HBM bytes per call of append and select, per chunk."""
         w = self.w
@@ -616,7 +624,11 @@ def main():
             return None
         t = sum(a.elapsed_time(b) for a, b, _ in events) * 1e-3
         return sum(nbytes[c] for _, _, c in events) / t / 1e9 if t > 0 else None
-    app_gbs, sel_gbs = gbs(step.app_events, app_b), gbs(step.sel_events, sel_b)
+    app_gbs = gbs(step.app_events, app_b)
+    # selection bandwidth over the calls that score pages (dense selections keep every
+    # page and the window selection reads nothing: their calls only write the set)
+    scored = step.scored_chunks()
+    sel_gbs = gbs([e for e in step.sel_events if e[2] in scored], sel_b) if scored else None
     # size-matched references (largest call of each kind)
     app_ref = same_size_gbs(max(app_b.values()), dev, "copy") if app_gbs else None
     sel_ref = same_size_gbs(max(sel_b.values()), dev, "read") if sel_gbs else None
@@ -714,7 +726,8 @@ def main():
                             "frac_of_same_size_copy": round(app_gbs / app_ref, 3) if app_ref else None,
                             "bytes_per_token_per_kv_head": 2 * 2 * w.head_dim * (2 if w.dtype == "bf16" else 4)
                             + 2 * w.head_dim * 4},
-            "select_call": {"gbs": round(sel_gbs, 1) if sel_gbs else None,
+            "select_call": {"scored_calls_per_step": len(scored),
+                            "gbs": round(sel_gbs, 1) if sel_gbs else None,
                             "frac_of_hbm": round(sel_gbs / hbm_peak, 3) if sel_gbs else None,
                             "same_size_read_gbs": round(sel_ref, 1) if sel_ref else None,
                             "frac_of_same_size_read": round(sel_gbs / sel_ref, 3) if sel_ref else None},
