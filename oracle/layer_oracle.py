@@ -13,15 +13,18 @@ recomputed on the fly just before the backward needs them; 2.B — K/V and their
 gradients live in pages and are accumulated in place; 2.D — top-K page retrieval
 (or, for the sparse layers of sparse-native models, a local window).
 
-Readings where the pages are silent (also in the design notes): the layer's
-trainable part on this path is the three projections Q = X Wq, K = X Wk,
-V = X Wv (no biases; the output projection and everything after it are outside
-the attention path, so the gradient arriving here is dO, the gradient of the loss
-with respect to the attention output); the rotary embedding is the rotate-half
-form with pairs (i, i + d/2) and angle position * theta^(-2i/d) at absolute
-positions (the form of the Qwen2.5 models the explainer's experiments use); K and
-V are kept in the pool between the sweeps (the KV cache), so the reverse sweep
-recomputes only the queries and the attention output.
+Readings where the pages are silent (also in the design notes):
+* the layer's trainable part on this path is the three projections
+  Q = X Wq + bq, K = X Wk + bk, V = X Wv + bv (the biases are optional; Qwen2.5's
+  projections carry them);
+* the output projection and everything after it lie outside the attention path,
+  so the gradient that arrives is dO, the gradient of the loss with respect to
+  the attention output;
+* the rotary embedding is the rotate-half form, pairs (i, i + d/2) turned by the
+  angle position * theta^(-2i/d) at absolute positions (the form of the Qwen2.5
+  models that the explainer's experiments use);
+* K and V stay in the pool between the sweeps (the KV cache), so the reverse
+  sweep recomputes only the queries and the attention output.
 
 Matrix products via numpy are the only library steps.
 """
@@ -55,7 +58,8 @@ def rope(x: np.ndarray, pos0: int, theta: float, inverse: bool = False) -> np.nd
 def layer_sweep(X: np.ndarray, Wq: np.ndarray, Wk: np.ndarray, Wv: np.ndarray, dO: np.ndarray,
                 n_q_heads: int, n_kv_heads: int, chunk: int, page: int, phys_order: Sequence[int],
                 scale: float, theta: float, top_k: int = -1, n_sink: int = 1,
-                window: Optional[int] = None, sel_override=None):
+                window: Optional[int] = None, sel_override=None, bq: Optional[np.ndarray] = None,
+                bk: Optional[np.ndarray] = None, bv: Optional[np.ndarray] = None):
     """One layer step over the whole sequence.
 
     X [N, Dm] (the layer's input activations), Wq [Dm, Hq*d], Wk and Wv
@@ -68,7 +72,10 @@ def layer_sweep(X: np.ndarray, Wq: np.ndarray, Wk: np.ndarray, Wv: np.ndarray, d
     later chunks, all done by now — the chunk's dK/dV complete: the gradients go
     back through the rotary embedding (its inverse rotation) and the projections.
 
-    Returns a dict: O (list per chunk), dX [N, Dm], dWq, dWk, dWv, sel.
+    bq [Hq*d], bk and bv [Hkv*d] are optional projection biases (None = none).
+
+    Returns a dict: O (list per chunk), dX [N, Dm], dWq, dWk, dWv, dbq, dbk, dbv
+    (zeros where there is no bias), sel.
     """
     N, Dm = X.shape
     Hq, Hkv = n_q_heads, n_kv_heads
@@ -80,14 +87,19 @@ def layer_sweep(X: np.ndarray, Wq: np.ndarray, Wk: np.ndarray, Wv: np.ndarray, d
     used = 0
     out = {"O": [], "sel": []}
 
+    zq, zk = np.zeros(Hq * d, F64), np.zeros(Hkv * d, F64)
+    bq = zq if bq is None else bq
+    bk = zk if bk is None else bk
+    bv = zk if bv is None else bv
+
     def project_q(s, n):
-        return rope((X[s:s + n] @ Wq).reshape(n, Hq, d), s, theta)
+        return rope((X[s:s + n] @ Wq + bq).reshape(n, Hq, d), s, theta)
 
     for s in starts:
         n = min(chunk, N - s)
         q = project_q(s, n)
-        k = rope((X[s:s + n] @ Wk).reshape(n, Hkv, d), s, theta)
-        v = (X[s:s + n] @ Wv).reshape(n, Hkv, d)
+        k = rope((X[s:s + n] @ Wk + bk).reshape(n, Hkv, d), s, theta)
+        v = (X[s:s + n] @ Wv + bv).reshape(n, Hkv, d)
         npg = (s + n - 1) // page - s // page + 1
         pool.append(k, v, s, order[used:used + npg])
         used += npg
@@ -104,6 +116,7 @@ def layer_sweep(X: np.ndarray, Wq: np.ndarray, Wk: np.ndarray, Wv: np.ndarray, d
 
     dX = np.zeros_like(X, dtype=F64)
     dWq, dWk, dWv = (np.zeros_like(W, dtype=F64) for W in (Wq, Wk, Wv))
+    dbq, dbk, dbv = np.zeros_like(zq), np.zeros_like(zk), np.zeros_like(zk)
     for ci in range(len(starts) - 1, -1, -1):
         s = starts[ci]
         n = min(chunk, N - s)
@@ -119,6 +132,9 @@ def layer_sweep(X: np.ndarray, Wq: np.ndarray, Wk: np.ndarray, Wv: np.ndarray, d
         dWq += xc.T @ gq
         dWk += xc.T @ gk
         dWv += xc.T @ gv
+        dbq += gq.sum(axis=0)
+        dbk += gk.sum(axis=0)
+        dbv += gv.sum(axis=0)
         dX[s:s + n] = gq @ Wq.T + gk @ Wk.T + gv @ Wv.T
-    out.update(dX=dX, dWq=dWq, dWk=dWk, dWv=dWv)
+    out.update(dX=dX, dWq=dWq, dWk=dWk, dWv=dWv, dbq=dbq, dbk=dbk, dbv=dbv)
     return out

@@ -54,14 +54,17 @@ def _rope_t(x, theta):
     return torch.cat([a * c - b * s, b * c + a * s], dim=-1)
 
 
-def _autograd_layer(X, Wq, Wk, Wv, dO, Hq, Hkv, scale, theta, mask):
+def _autograd_layer(X, Wq, Wk, Wv, dO, Hq, Hkv, scale, theta, mask, bq=None, bk=None, bv=None):
     """Unchunked layer with torch autograd; mask [Hq, N, N] (True = visible)."""
-    t = {k: torch.tensor(v, requires_grad=True) for k, v in dict(X=X, Wq=Wq, Wk=Wk, Wv=Wv).items()}
     N = X.shape[0]
     d = Wq.shape[1] // Hq
-    q = _rope_t((t["X"] @ t["Wq"]).reshape(N, Hq, d), theta)
-    k = _rope_t((t["X"] @ t["Wk"]).reshape(N, Hkv, d), theta)
-    v = (t["X"] @ t["Wv"]).reshape(N, Hkv, d)
+    zq, zk = np.zeros(Hq * d), np.zeros(Hkv * d)
+    src = dict(X=X, Wq=Wq, Wk=Wk, Wv=Wv, bq=zq if bq is None else bq, bk=zk if bk is None else bk,
+               bv=zk if bv is None else bv)
+    t = {k: torch.tensor(v, requires_grad=True) for k, v in src.items()}
+    q = _rope_t((t["X"] @ t["Wq"] + t["bq"]).reshape(N, Hq, d), theta)
+    k = _rope_t((t["X"] @ t["Wk"] + t["bk"]).reshape(N, Hkv, d), theta)
+    v = (t["X"] @ t["Wv"] + t["bv"]).reshape(N, Hkv, d)
     G = Hq // Hkv
     o = torch.nn.functional.scaled_dot_product_attention(
         q.transpose(0, 1)[None], k.transpose(0, 1).repeat_interleave(G, 0)[None],
@@ -95,22 +98,29 @@ def _problem(seed, N, Dm, Hq, Hkv, d):
     return rng, X, Wq, Wk, Wv, dO
 
 
-@pytest.mark.parametrize("kind", ["dense", "topk", "window"])
+@pytest.mark.parametrize("kind", ["dense", "topk", "window", "biased"])
 def test_layer_step_equals_unchunked_autograd(kind):
     N, C, P, Hq, Hkv, d, Dm = 56, 16, 4, 4, 2, 8, 12
     theta = 1e4
     rng, X, Wq, Wk, Wv, dO = _problem(11, N, Dm, Hq, Hkv, d)
     scale = 1.0 / math.sqrt(d)
     order = rng.permutation(N // P + 2)
-    kw = dict(top_k=-1) if kind == "dense" else dict(top_k=3) if kind == "topk" else dict(window=2)
-    res = LO.layer_sweep(X, Wq, Wk, Wv, dO, Hq, Hkv, C, P, order, scale, theta, n_sink=1, **kw)
-    if kind == "topk":  # the selection really drops pages
+    kw = dict(top_k=-1) if kind == "dense" else dict(window=2) if kind == "window" else dict(top_k=3)
+    bias = {}
+    if kind == "biased":  # Qwen2.5-style projection biases, with a sparse selection
+        bias = dict(bq=rng.standard_normal(Hq * d), bk=rng.standard_normal(Hkv * d),
+                    bv=rng.standard_normal(Hkv * d))
+    res = LO.layer_sweep(X, Wq, Wk, Wv, dO, Hq, Hkv, C, P, order, scale, theta, n_sink=1, **kw, **bias)
+    if kind in ("topk", "biased"):  # the selection really drops pages
         assert len(res["sel"][-1][0]) < N // P
     mask = _mask_from_selection(res["sel"], N, C, P, Hq, Hkv)
-    o_ref, g = _autograd_layer(X, Wq, Wk, Wv, dO, Hq, Hkv, scale, theta, mask)
+    o_ref, g = _autograd_layer(X, Wq, Wk, Wv, dO, Hq, Hkv, scale, theta, mask, **bias)
     assert O.rel_l2(np.concatenate(res["O"]), o_ref) < 1e-12
     for name in ("X", "Wq", "Wk", "Wv"):
         assert O.rel_l2(res["d" + name], g[name]) < 1e-12, name
+    if bias:
+        for name in ("bq", "bk", "bv"):
+            assert O.rel_l2(res["d" + name], g[name]) < 1e-12, name
 
 
 def test_layer_step_finite_differences():
