@@ -72,3 +72,26 @@ def test_dense_credit_closed_form():
     for c in range(w.n_chunks):
         start, n = w.chunk_bounds(c)
         assert got[c] == sum(start + i + 1 for i in range(n)) * w.n_q_heads
+
+
+def test_algorithmic_bytes_per_call():
+    """Append: 2 KB per token and KV head at d = 128 (K, V read and written in bf16,
+    both fp32 gradient rows zeroed) plus the 512-byte summary row of each page and
+    head; selection: the chunk's Q once, each candidate's summary row once, plus the
+    written set; state per 10K tokens: K/V bf16 + dK/dV fp32 + summaries (K/V on
+    the host with offload)."""
+    w = synth.WORKLOADS["sparse128k"]
+    ns = types.SimpleNamespace(w=w)
+    app, sel = bench.Step.hbm_bytes(ns)
+    C, Hkv, Hq, d, P = w.chunk, w.n_kv_heads, w.n_q_heads, w.head_dim, w.page
+    assert app[5] == C * Hkv * 2048 + (C // P) * Hkv * d * 4
+    c = w.n_chunks - 1
+    n_cand = c * C // P - w.n_sink
+    assert sel[c] == C * Hq * d * 2 + n_cand * Hkv * d * 4 + 2 * n_cand * Hkv * 4 + Hkv * w.max_sel * 4
+    assert sel[0] == Hkv * w.max_sel * 4  # nothing to score in the first chunk
+    st = bench.state_bytes_per_10k(w)
+    # the summary row of a page is shared by its P tokens: d * 4 / P bytes per token and head
+    assert st["device"] == 10_000 * Hkv * d * (2 * 2 + 2 * 4) + 10_000 * Hkv * d * 4 // P
+    assert st["host"] == 0
+    off = bench.state_bytes_per_10k(synth.WORKLOADS["offload4m"])  # K/V move to pinned host memory
+    assert off["host"] == 10_000 * Hkv * d * 2 * 2 and off["device"] == st["device"] - off["host"]
