@@ -118,9 +118,10 @@ class Step:
         self.scale = 1.0 / math.sqrt(w.head_dim)
         order = synth.page_order(w)
         self.offload = bool(w.offload)
+        self.offload_grads = bool(w.offload and w.offload_grads)
         self.pool = PagedKVPool(w.n_q_heads, w.n_kv_heads, w.head_dim, w.page, w.num_phys, w.n_pages,
                                 w.torch_dtype, dev, page_order=order, offload=self.offload,
-                                stage_max_sel=w.max_sel if self.offload else 0)
+                                stage_max_sel=w.max_sel if self.offload else 0, offload_grads=self.offload_grads)
         plants = synth.PlantTable(w) if w.plants > 0 else None
         # inputs generated per chunk (seeded) on the device -- or on the host and uploaded,
         # keeping the host copies, when a test needs the same tensors for the oracle --
@@ -146,7 +147,10 @@ class Step:
         self.dq = [torch.empty_like(ch["q"]) for ch in self.chunks]
         self.fwd_events, self.bwd_events, self.app_events, self.sel_events = [], [], [], []
         self.recompute_events, self.prefetch_events = [], []  # reverse-sweep forwards; offload copies
-        self.side = torch.cuda.Stream(device=dev) if self.offload else None
+        # the side stream runs at high priority: the block scheduler then places its small
+        # transfer blocks beside the attention CTAs at once, instead of after the last of
+        # a long attention grid's pending blocks
+        self.side = torch.cuda.Stream(device=dev, priority=-1) if self.offload else None
 
     def run(self, record=False, no_recompute=False, wait_in=None, on_dq=None):
         """One step.  The reverse sweep recomputes each chunk's O and LSE (activations are
@@ -155,7 +159,7 @@ class Step:
         wait_in[c]: an event the step waits for before it first reads chunk c's inputs;
         on_dq(c): called once chunk c's dQ has been issued (end-to-end copies)."""
         if self.offload:
-            return self.run_offload(record)
+            return self.run_offload(record, wait_in=wait_in, on_dq=on_dq)
         L, w, h, torch = self.L, self.w, self.pool.handle, self.torch
         L.oomb_pool_reset(h)
         for c, ch in enumerate(self.chunks):
@@ -186,49 +190,67 @@ class Step:
             if on_dq is not None:
                 on_dq(c)
 
-    def run_offload(self, record=False):
-        """K/V pools in pinned host memory.  The side stream gathers the selected pages
-        of the next chunk into the other staging buffer while the main stream runs the
-        current chunk's attention (forward sweep: chunk c+1 is appended and selected
-        before chunk c's forward; reverse sweep: chunk c-1 is gathered during chunk c)."""
+    def run_offload(self, record=False, wait_in=None, on_dq=None):
+        """K/V pools (and, with offload_grads, the fp32 dK/dV pools) in pinned host memory.
+        The side stream moves the selected blocks of the next chunk into the other
+        staging buffer while the main stream runs the current chunk's attention (forward
+        sweep: chunk c+1 is appended and selected before chunk c's forward; reverse sweep:
+        chunk c-1's K/V and the gradient blocks it does not share with chunk c are
+        staged during chunk c's backward; after it, the shared blocks are carried over
+        from chunk c's staging and chunk c's blocks are written back to the host)."""
         L, w, h, torch = self.L, self.w, self.pool.handle, self.torch
         main, side = torch.cuda.current_stream(self.dev), self.side
         S = w.n_chunks
+        grads = self.offload_grads
         ev = lambda: torch.cuda.Event()  # noqa: E731
         L.oomb_pool_reset(h)
 
         def append_select(c):
             start, n = w.chunk_bounds(c)
             ch = self.chunks[c]
+            if wait_in is not None:
+                main.wait_event(wait_in[c])
             self._timed(record, self.app_events, c, L.oomb_kv_append, h, ch["k"], ch["v"], start)
             self._select(c, ch, start, n, record)
 
-        def prefetch(c, after):
-            for e in after:
-                side.wait_event(e)
+        def side_timed(c, fn):
             if record:
                 p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 p0.record(side)
-            L.oomb_prefetch(h, self.sel[c], self.cnt[c], c % 2, stream=side)
+            fn()
             if record:
                 p1.record(side)
                 self.prefetch_events.append((p0, p1, c))
+
+        def prefetch(c, after, prev=None):
+            """K/V of chunk c (and in the reverse sweep its gradient blocks not shared
+            with chunk prev) into staging buffer c % 2; returns the side-stream event."""
+            for e in after:
+                side.wait_event(e)
+
+            def work():
+                L.oomb_prefetch(h, self.sel[c], self.cnt[c], c % 2, stream=side)
+                if prev is not False and grads:
+                    psel = self.sel[prev] if prev is not None else None
+                    pcnt = self.cnt[prev] if prev is not None else None
+                    L.oomb_grad_prefetch(h, self.sel[c], self.cnt[c], psel, pcnt, c % 2, stream=side)
+            side_timed(c, work)
             done = ev()
             done.record(side)
             return done
 
-        # forward sweep
+        # forward sweep (K/V only)
         append_select(0)
         sel_ev = ev()
         sel_ev.record(main)
-        pf = {0: prefetch(0, [sel_ev])}
+        pf = {0: prefetch(0, [sel_ev], prev=False)}
         used = {}
         for c in range(S):
             if c + 1 < S:
                 append_select(c + 1)
                 e = ev()
                 e.record(main)
-                pf[c + 1] = prefetch(c + 1, [e] + ([used[c - 1]] if c - 1 in used else []))
+                pf[c + 1] = prefetch(c + 1, [e] + ([used[c - 1]] if c - 1 in used else []), prev=False)
             main.wait_event(pf[c])
             L.oomb_pool_set_stage(h, c % 2)
             start, n = w.chunk_bounds(c)
@@ -236,17 +258,28 @@ class Step:
             used[c] = ev()
             used[c].record(main)
         # reverse sweep
-        pf = {S - 1: prefetch(S - 1, [used[S - 1]])}
+        ready = {S - 1: prefetch(S - 1, [used[S - 1]], prev=None)}
         for c in range(S - 1, -1, -1):
-            if c - 1 >= 0:
-                pf[c - 1] = prefetch(c - 1, [used[c + 1]] if c + 1 < S else [used[S - 1]])
-            main.wait_event(pf[c])
+            if c - 1 >= 0:  # buffer (c-1) % 2 was last used by chunk c+1 (or, first, the forward sweep)
+                ready[c - 1] = prefetch(c - 1, [used[c + 1]] if c + 1 < S else [used[S - 1]], prev=c)
+            main.wait_event(ready[c])
             L.oomb_pool_set_stage(h, c % 2)
             start, n = w.chunk_bounds(c)
             self._fwd(c, self.chunks[c], start, n, record, recompute=True)
             self._bwd(c, self.chunks[c], start, n, record)
             used[c] = ev()
             used[c].record(main)
+            if on_dq is not None:
+                on_dq(c)
+            if grads:
+                side.wait_event(used[c])
+                if c - 1 >= 0:  # blocks of chunk c-1 also selected by chunk c: carried over
+                    side_timed(c - 1, lambda: L.oomb_grad_carry(h, self.sel[c - 1], self.cnt[c - 1], self.sel[c],
+                                                                self.cnt[c], (c - 1) % 2, stream=side))
+                    ready[c - 1] = ev()
+                    ready[c - 1].record(side)
+                side_timed(c, lambda: L.oomb_grad_writeback(h, self.sel[c], self.cnt[c], c % 2, stream=side))
+        main.wait_stream(side)  # the last write-backs belong to the step
 
     def _timed(self, record, events, c, fn, *args):
         if not record:
@@ -357,14 +390,31 @@ def state_bytes_per_10k(w) -> dict:
     """Device bytes of one layer's attention state that grow with the context, per
     10,000 tokens: K/V pools, fp32 dK/dV pools and the page summaries (the analogue,
     for this path alone, of the pages' end-to-end memory growth per 10K tokens).
-    With offload the K/V pools live in host memory and only a fixed staging buffer is
-    on the device."""
+    With offload the K/V pools (and with offload_grads the gradient pools) live in
+    host memory and only fixed staging buffers are on the device."""
     esz = 2 if w.dtype == "bf16" else 4
     per_tok_kv = 2 * w.n_kv_heads * w.head_dim * esz
     per_tok_grad = 2 * w.n_kv_heads * w.head_dim * 4
     per_tok_sum = w.n_kv_heads * w.head_dim * 4 / w.page
-    dev = per_tok_grad + per_tok_sum + (0 if w.offload else per_tok_kv)
-    return {"device": int(dev * 10000), "host": int(per_tok_kv * 10000) if w.offload else 0}
+    host = (per_tok_kv if w.offload else 0) + (per_tok_grad if w.offload and w.offload_grads else 0)
+    dev = per_tok_kv + per_tok_grad + per_tok_sum - host
+    stage = 0
+    if w.offload:  # two staging buffers of max_sel blocks per KV head: K/V, and fp32 dK/dV
+        blk = w.page * w.head_dim
+        stage = 2 * w.n_kv_heads * w.max_sel * blk * (2 * esz + (2 * 4 if w.offload_grads else 0))
+    return {"device": int(dev * 10000), "host": int(host * 10000), "fixed_staging_device": int(stage)}
+
+
+def config_of(w, world: int) -> dict:
+    """The `config` of the JSON line, the same for both arms."""
+    tc = w.dtype == "bf16" and w.head_dim == 128 and w.page == 128
+    return {"workload": w.name, "seq": w.seq, "chunk": w.chunk, "page": w.page, "top_k": w.top_k,
+            **({"window_pages": w.window, "n_sink": w.n_sink} if w.window >= 0 else {}),
+            "heads": f"{w.n_q_heads}/{w.n_kv_heads}", "head_dim": w.head_dim,
+            "offload": ("kv+grads" if w.offload_grads else "kv") if w.offload else "none",
+            "parallelism": "replicas" if world > 1 else "single",
+            "l2": "inputs larger than L2 (Q+dO of one chunk alone exceed 58 MB; all chunks resident)",
+            "attention_kernels": "tcgen05" if tc else "simt"}
 
 
 def recorded_traffic(workload: str, kernel: str):
@@ -523,9 +573,7 @@ def run_reference(args, w, rank, world):
     line = {"impl": "reference", "metric": METRIC, "value": tflops, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "seq": w.seq, "chunk": w.chunk, "page": w.page, "top_k": w.top_k,
-                       **({"window_pages": w.window, "n_sink": w.n_sink} if w.window >= 0 else {}),
-                       "heads": f"{w.n_q_heads}/{w.n_kv_heads}", "head_dim": w.head_dim},
+            "config": config_of(w, world),
             "cpu_baseline": {"value": tflops, "unit": UNIT, "cores": res[0]["cores"], "kind": "oracle",
                              "sample": res[0]["sample"]},
             "e2e": {"value": tflops, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -538,7 +586,7 @@ def main():
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="oomb", choices=["oomb", "reference"])
-    ap.add_argument("--workload", default="dense32k")
+    ap.add_argument("--workload", default="offload4m")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
@@ -617,7 +665,10 @@ def main():
     peaks = load_peaks()
     bwd_tflops = sum(bwd_fl) / (sum(bwd_ms) * 1e-3) / 1e12
     fwd_tflops = sum(fwd_fl) / (sum(fwd_ms) * 1e-3) / 1e12
-    peak = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
+    # per-call event timings of one kernel: the burst GEMM peak; the whole seconds-long
+    # step is also given against the sustained one
+    peak = peaks.get("bf16_tflops", 1900.0)
+    peak_sustained = peaks.get("bf16_tflops_sustained", peak)
     app_b, sel_b = step.hbm_bytes()
     def gbs(events, nbytes):
         if not events:
@@ -651,19 +702,31 @@ def main():
     kern_ms = sum(a.elapsed_time(b) for ev in (step.fwd_events, step.bwd_events, step.app_events, step.sel_events)
                   for a, b, _ in ev) / args.steps
     prefetch = None
-    if step.prefetch_events:
-        import torch as _t
+    if step.offload:
+        import numpy as np
         esz = 2 if w.dtype == "bf16" else 4
-        cnt = step.cnt.cpu()
-        pf_bytes = {c: int(cnt[c].sum()) * w.page * w.head_dim * 2 * esz for c in range(w.n_chunks)}
-        pf_s = sum(a.elapsed_time(b) for a, b, _ in step.prefetch_events) * 1e-3
-        pf_b = sum(pf_bytes[c] for _, _, c in step.prefetch_events)
-        # isolated: each of the last chunks' gathers three times in a row (the first
+        S, Hkv = w.n_chunks, w.n_kv_heads
+        sel_h, cnt_h = step.sel.cpu().numpy(), step.cnt.cpu().numpy()
+        sets = [[set(sel_h[c, hk, : int(cnt_h[c, hk])].tolist()) for hk in range(Hkv)] for c in range(S)]
+        n_blk = [sum(len(x) for x in sets[c]) for c in range(S)]
+        kv_blk = 2 * w.page * w.head_dim * esz   # K and V of one (page, KV head)
+        g_blk = 2 * w.page * w.head_dim * 4      # dK and dV
+        kv_in = 2 * sum(n_blk) * kv_blk           # both sweeps
+        g_in = g_out = carried = 0
+        if step.offload_grads:
+            for c in range(S):
+                shared = sum(len(sets[c][hk] & sets[c + 1][hk]) for hk in range(Hkv)) if c + 1 < S else 0
+                g_in += (n_blk[c] - shared) * g_blk
+                carried += shared * g_blk
+                g_out += n_blk[c] * g_blk
+        link_b = kv_in + g_in + g_out
+        pf_s = sum(a.elapsed_time(b) for a, b, _ in step.prefetch_events) * 1e-3 / args.steps
+        # isolated: each of the last chunks' K/V gathers three times in a row (the first
         # gather of a page set after the step can take far longer than the repeats,
         # so it is reported on its own; the repeats give the gather's bandwidth), and
         # a plain pinned-host -> HBM copy for the link's bandwidth
         iso, first_ms = [], []
-        for c in range(max(0, w.n_chunks - 3), w.n_chunks):
+        for c in range(max(0, S - 3), S):
             for rep in range(3):
                 torch.cuda.synchronize()
                 g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -675,7 +738,7 @@ def main():
                 if rep == 0:
                     first_ms.append(round(t, 3))
                 else:
-                    iso.append(pf_bytes[c] / (t * 1e-3) / 1e9)
+                    iso.append(n_blk[c] * kv_blk / (t * 1e-3) / 1e9)
         hbuf = torch.empty(256 << 20, dtype=torch.uint8).pin_memory()
         dbuf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
         dbuf.copy_(hbuf)
@@ -687,37 +750,41 @@ def main():
         c1.record()
         torch.cuda.synchronize()
         link = 4 * (256 << 20) / (c0.elapsed_time(c1) * 1e-3) / 1e9
-        prefetch = {"gbs_overlapped": round(pf_b / pf_s / 1e9, 1),
-                    "gbs_isolated": round(statistics.median(iso), 1),
+        del hbuf, dbuf
+        prefetch = {"link": "pinned host memory <-> HBM staging over NVLink-C2C (side stream, zero-copy kernels)",
+                    "host_bytes_per_step": {"kv_in": kv_in, "grad_in": g_in, "grad_out": g_out,
+                                            "grad_carried_on_device": carried},
+                    "gbs_overlapped": round(link_b / pf_s / 1e9, 1) if pf_s > 0 else None,
+                    "gbs_isolated_kv_gather": round(statistics.median(iso), 1),
                     "isolated_first_call_ms": first_ms,
                     "host_link_copy_gbs": round(link, 1),
-                    "bytes_per_chunk_max": max(pf_bytes.values()),
-                    "link": "pinned host memory -> HBM staging (side stream)",
-                    "side_stream_ms_per_step": round(pf_s * 1e3 / args.steps, 3),
+                    "side_stream_ms_per_step": round(pf_s * 1e3, 3),
                     "main_stream_kernel_ms_per_step": round(kern_ms, 3),
-                    "exposed_ms_per_step": round(max(0.0, ms - kern_ms), 3)}
+                    "exposed_ms_per_step": round(max(0.0, ms - kern_ms), 3),
+                    "exposed_frac_of_step": round(max(0.0, ms - kern_ms) / ms, 4)}
 
     line = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": max(3, args.warmup), "ms_per_step": round(ms, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "fp32",
             "data": "synthetic (seeded N(0,1) Q/K/V/dO, RoPE theta 1e6; no trained weights)",
-            "config": {"workload": w.name, "seq": w.seq, "chunk": w.chunk, "page": w.page, "top_k": w.top_k,
-                       **({"window_pages": w.window, "n_sink": w.n_sink} if w.window >= 0 else {}),
-                       "heads": f"{w.n_q_heads}/{w.n_kv_heads}", "head_dim": w.head_dim,
-                       "parallelism": "replicas" if world > 1 else "single",
-                       "l2": "inputs larger than L2 (Q+dO alone exceed 129 MB)",
-                       "attention_kernels": "tcgen05" if L.oomb_uses_tensor_cores(step.pool.handle) else "simt"},
+            "config": config_of(w, world),
             "tokens_per_s_per_layer": round(tokens_per_s, 1),
             "tokens_per_s_per_layer_no_recompute": round(job_throughput(w.seq, nr_ms, world), 1) if nr_ms else None,
             "ms_per_step_no_recompute": round(nr_ms, 3) if nr_ms else None,
             "recompute_call_ms_per_step": round(rec_ms, 3),
             "credited_tflop_per_step": credited / 1e12,
             "value_frac_of_peak": round(value / peak, 4),
+            "value_frac_of_sustained_peak": round(value / peak_sustained, 4),
             "state_bytes_per_10k_tokens": state_bytes_per_10k(w),
             "fwd_call_tflops": round(fwd_tflops, 2), "bwd_call_tflops": round(bwd_tflops, 2),
+            "fwd_bwd_call_tflops": round((sum(fwd_fl) + sum(bwd_fl)) / ((sum(fwd_ms) + sum(bwd_ms)) * 1e-3) / 1e12, 2),
             "roofline": {"bound": "tensor", "kernel": "oomb_chunk_attn_bwd", "achieved": round(bwd_tflops, 2),
                          "peak": peak, "unit": "TFLOP/s", "frac": round(bwd_tflops / peak, 4),
-                         "peak_source": peaks.get("source", "") + " (bf16 dense, sustained)",
+                         "frac_of_sustained": round(bwd_tflops / peak_sustained, 4),
+                         "fwd_frac": round(fwd_tflops / peak, 4),
+                         "fwd_bwd_frac": round((sum(fwd_fl) + sum(bwd_fl)) / ((sum(fwd_ms) + sum(bwd_ms)) * 1e-3)
+                                               / 1e12 / peak, 4),
+                         "peak_source": peaks.get("source", "") + " (bf16 dense, burst; per-call event timings)",
                          "traffic": recorded_traffic(w.name, "oomb_chunk_attn_bwd"),
                          "traffic_unit": "DRAM bytes per launch (ncu dram__bytes_read.sum + write.sum)"},
             "append_call": {"gbs": round(app_gbs, 1) if app_gbs else None,
@@ -749,19 +816,66 @@ def main():
         dist.destroy_process_group()
 
 
+class HostBuffer:
+    """One page-locked host allocation holding many tensors.  Plain pageable memory
+    registered with cudaHostRegister: exactly the bytes asked for (the caching pinned
+    allocator rounds each block up to a power of two, which would nearly double a
+    ~70 GB set of inputs), and async copies to and from it run at the link's speed."""
+
+    def __init__(self, nbytes: int):
+        import torch
+        self.buf = torch.empty(max(16, nbytes), dtype=torch.uint8)
+        self.off = 0
+        err = torch.cuda.cudart().cudaHostRegister(self.buf.data_ptr(), self.buf.numel(), 0)
+        if int(err) != 0:
+            raise RuntimeError(f"cudaHostRegister failed ({err})")
+
+    def take(self, shape, dtype):
+        import torch
+        n = int(math.prod(shape)) * torch.tensor([], dtype=dtype).element_size()
+        self.off = (self.off + 255) // 256 * 256
+        t = self.buf[self.off:self.off + n].view(dtype).view(shape)
+        self.off += n
+        return t
+
+    def close(self):
+        import torch
+        if self.buf is not None:
+            torch.cuda.synchronize()
+            torch.cuda.cudart().cudaHostUnregister(self.buf.data_ptr())
+            self.buf = None
+
+
 def measure_e2e(step, steps, credited, world, dev):
     """Same step with host-resident inputs: every step copies Q, K, V, dO of all
-    chunks from pinned host memory to the device and reads dQ and the dK/dV pools
-    back, all inside the timed region.  The uploads run on a copy stream, chunk by
-    chunk, and each chunk waits only for its own inputs; each dQ is read back on the
-    copy stream as soon as its backward is issued (the pools at the end of the step)."""
+    chunks from page-locked host memory to the device and reads dQ (and, when the
+    gradient pools are in HBM, dK/dV) back, all inside the timed region.  The uploads
+    run on a copy stream, chunk by chunk, and each chunk waits only for its own
+    inputs; each dQ is read back on the copy stream as soon as its backward is issued
+    (the pools at the end of the step).  With offloaded gradient pools the step's own
+    write-backs put dK/dV in host memory; those bytes are counted as read back."""
     import torch
-    host_in = [{k: v.cpu().pin_memory() for k, v in ch.items()} for ch in step.chunks]
-    host_dq = [torch.empty(d.shape, dtype=d.dtype).pin_memory() for d in step.dq]
-    host_dk = torch.empty(step.pool.dk_pool.shape, dtype=torch.float32).pin_memory()
-    host_dv = torch.empty(step.pool.dv_pool.shape, dtype=torch.float32).pin_memory()
-    bi = sum(t.numel() * t.element_size() for ch in host_in for t in ch.values())
-    bo = sum(t.numel() * t.element_size() for t in host_dq) + 2 * host_dk.numel() * 4
+    sizes = [t.numel() * t.element_size() for ch in step.chunks for t in ch.values()]
+    dq_sizes = [d.numel() * d.element_size() for d in step.dq]
+    hb = HostBuffer(sum(sizes) + sum(dq_sizes) + 256 * (len(sizes) + len(dq_sizes)))
+    host_in = [{k: hb.take(v.shape, v.dtype) for k, v in ch.items()} for ch in step.chunks]
+    for ch, hc in zip(step.chunks, host_in):
+        for k in ch:
+            hc[k].copy_(ch[k])
+    host_dq = [hb.take(d.shape, d.dtype) for d in step.dq]
+    pools_on_device = not step.offload_grads
+    host_dk = host_dv = None
+    if pools_on_device:
+        hp = HostBuffer(2 * step.pool.dk_pool.numel() * 4 + 512)
+        host_dk = hp.take(step.pool.dk_pool.shape, torch.float32)
+        host_dv = hp.take(step.pool.dv_pool.shape, torch.float32)
+    torch.cuda.synchronize()
+    bi = sum(sizes)
+    bo = sum(dq_sizes) + (2 * host_dk.numel() * 4 if pools_on_device else 0)
+    if not pools_on_device:  # the reverse sweep's gradient write-backs (each selected block, dK and dV)
+        w = step.w
+        cnt_h = step.cnt.cpu()
+        bo += int(cnt_h.sum()) * 2 * w.page * w.head_dim * 4
     main = torch.cuda.current_stream(dev)
     copy = torch.cuda.Stream(device=dev)
 
@@ -783,10 +897,11 @@ def measure_e2e(step, steps, credited, world, dev):
                 host_dq[c].copy_(step.dq[c], non_blocking=True)
 
         step.run(wait_in=ready, on_dq=on_dq)
-        copy.wait_stream(main)
-        with torch.cuda.stream(copy):
-            host_dk.copy_(step.pool.dk_pool, non_blocking=True)
-            host_dv.copy_(step.pool.dv_pool, non_blocking=True)
+        if pools_on_device:
+            copy.wait_stream(main)
+            with torch.cuda.stream(copy):
+                host_dk.copy_(step.pool.dk_pool, non_blocking=True)
+                host_dv.copy_(step.pool.dv_pool, non_blocking=True)
         main.wait_stream(copy)
 
     one_step()  # warm-up of the copy path
@@ -798,6 +913,9 @@ def measure_e2e(step, steps, credited, world, dev):
     e1.record()
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
+    hb.close()
+    if pools_on_device:
+        hp.close()
     return {"value": round(credited / (ms * 1e-3) / 1e12 * world, 3), "unit": UNIT, "ms_per_step": round(ms, 3),
             "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
             "overlap": "uploads per chunk on a copy stream; dQ read back as each backward is issued"}

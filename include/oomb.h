@@ -101,7 +101,8 @@ typedef struct {
   int dtype;             /* oomb_dtype of K/V pools, Q, O, dO, dQ */
   void* k_pool;          /* [num_phys, Hkv, P, d]; device, or pinned+mapped host if offload */
   void* v_pool;          /* same */
-  float* dk_pool;        /* [num_phys, Hkv, P, d] fp32 device */
+  float* dk_pool;        /* [num_phys, Hkv, P, d] fp32; device, or pinned+mapped host
+                            if offload_grads */
   float* dv_pool;        /* same */
   float* summary;        /* [num_phys, Hkv, d] fp32 device */
   int32_t* page_table;   /* [max_logical_pages] device; written by the library */
@@ -114,6 +115,17 @@ typedef struct {
   void* stage_k;         /* offload only: [2, Hkv, stage_max_sel, P, d] device */
   void* stage_v;         /* same */
   int stage_max_sel;     /* offload only: selection capacity per KV head */
+  int offload_grads;     /* 1 (needs offload = 1): dk_pool/dv_pool live in pinned host
+                            memory too; the backward adds into the staged blocks
+                            stage_dk/stage_dv, which oomb_grad_prefetch/carry fill and
+                            oomb_grad_writeback returns to the host pools */
+  float* stage_dk;       /* offload_grads only: [2, Hkv, stage_max_sel, P, d] fp32 device */
+  float* stage_dv;       /* same */
+  uint8_t* grad_state;   /* offload_grads only: [num_phys, Hkv] device bytes, owned by the
+                            library: 0 = the host gradient block holds nothing yet (its
+                            page was appended and no write-back has reached it; it counts
+                            as zero and the append does not write the host block), 1 = the
+                            host block holds the gradient written back last */
 } oomb_pool_desc;
 
 typedef struct oomb_pool oomb_pool;
@@ -147,7 +159,9 @@ OOMB_API oomb_status oomb_page_free(oomb_pool* pool, int64_t first_logical_page,
  * copying of earlier pages).  Opens ceil((first_token+n)/P) - first_token/P new
  * logical pages, taking physical pages from the free list and writing their
  * page-table entries; copies k, v ([n_tokens, Hkv, d], dtype, device) into the
- * pools; zeroes the dK/dV rows of the written tokens; writes the page summary
+ * pools; zeroes the dK/dV rows of the written tokens (with offload_grads: marks
+ * the pages' host gradient blocks as holding nothing yet, see grad_state); writes
+ * the page summary
  * (fp32 mean key over the tokens present) of every touched page.
  * first_token must equal the tokens already appended and be a multiple of P.
  * Errors: ARG, ALIGN, OUT_OF_PAGES (nothing is written), CUDA. */
@@ -238,13 +252,19 @@ OOMB_API oomb_status oomb_chunk_attn_fwd(oomb_pool* pool, const void* q, int64_t
  * dP = dO V^T, D_i = dO_i . O_i, dS = P (dP - D):
  *   dq = scale dS K (written, dtype),
  *   dK_pool[phi(p), h] += scale dS^T Q,  dV_pool[phi(p), h] += P^T dO
- * summed over the G query heads of KV head h and every row of the chunk.
- * Summation order: on the tensor-core path (bf16, head_dim = page = 128) the
- * work of each (page, KV head) block is split over 2-4 thread blocks that add
- * their partial dK/dV with float reductions, and dq is accumulated in fp32 across
- * thread blocks, so repeated runs agree to rounding, not bit for bit; the SIMT
- * path (other shapes, fp32) gives each gradient row one owner and is
- * deterministic.  Backward calls on one pool must be stream-ordered.
+ * summed over the G query heads of KV head h and every row of the chunk (with
+ * offload_grads, into the staged blocks of buffer oomb_pool_set_stage()).
+ * Summation order: dK/dV are partitioned by (page, KV head).  On the tensor-core
+ * path (bf16, head_dim = page = 128) the work of a block is split over the 2-4
+ * thread blocks of one cluster, whose partials are summed in a fixed order in
+ * distributed shared memory and added once into the pool rows: no atomics on the
+ * gradient pool, and dK/dV are bit-identical from run to run.  dq is accumulated
+ * in fp32 across thread blocks with float reductions, so repeated runs agree to
+ * rounding, not bit for bit.  The SIMT path (other shapes, fp32) gives each
+ * gradient row one owner and is deterministic.  Backward calls on one pool must
+ * be stream-ordered.  The selection is checked on the device (count within
+ * [0, max_sel], entries strictly ascending and inside the chunk's view); a bad one
+ * sets OOMB_DEVERR_SEL and the affected pages are skipped, as in the forward.
  * Workspace: oomb_workspace_size(OOMB_OP_BWD, n_q) bytes, contents scratch.
  * Errors: ARG, ALIGN, WORKSPACE, UNSUPPORTED, CUDA. */
 OOMB_API oomb_status oomb_chunk_attn_bwd(oomb_pool* pool, const void* q, const void* o, const void* d_o, const float* lse,
@@ -260,7 +280,43 @@ OOMB_API oomb_status oomb_chunk_attn_bwd(oomb_pool* pool, const void* q, const v
 OOMB_API oomb_status oomb_prefetch(oomb_pool* pool, const int32_t* sel, const int32_t* sel_count, int max_sel,
                           int stage_buf, void* stream);
 
-/* Offload mode: staging buffer that following attention calls read. */
+/* Gradient offload (explainer 2.C: the KV cache and its gradients are moved
+ * between CPU and GPU memory; 2.B: gradient pages share the KV page table).  Needs offload_grads.
+ * In the reverse sweep the backward of chunk c adds into the staged dK/dV blocks
+ * of its selection (staging buffer c % 2, slot (h, s) as for K/V).  The three
+ * calls below fill and drain those slots; `prev_sel/prev_count` is the selection
+ * of the chunk whose backward ran just before (chunk c + 1, staged in buffer
+ * 1 - stage_buf), NULL for the first chunk of the sweep.  max_sel is the row
+ * length of sel and of prev_sel.
+ *
+ * oomb_grad_prefetch: stage the blocks of `sel` whose page is not in prev_sel
+ * from the host pools into buffer stage_buf (zero-filled where grad_state is 0).  Those host blocks are final with
+ * respect to the previous chunk, so this may run while the previous chunk's
+ * backward runs (order it after the previous write-backs: same stream).
+ * Errors: ARG, ALIGN, UNSUPPORTED (no offload_grads), CUDA. */
+OOMB_API oomb_status oomb_grad_prefetch(oomb_pool* pool, const int32_t* sel, const int32_t* sel_count, int max_sel,
+                                        const int32_t* prev_sel, const int32_t* prev_count, int stage_buf,
+                                        void* stream);
+
+/* oomb_grad_carry: copy the blocks of `sel` whose page is also in prev_sel from
+ * the previous chunk's staging buffer (1 - stage_buf) into buffer stage_buf, so
+ * that they carry the previous chunk's contribution without a round trip through
+ * host memory.  Must run after the previous chunk's backward and before this
+ * chunk's.  Errors: those of oomb_grad_prefetch (prev_sel is required). */
+OOMB_API oomb_status oomb_grad_carry(oomb_pool* pool, const int32_t* sel, const int32_t* sel_count, int max_sel,
+                                     const int32_t* prev_sel, const int32_t* prev_count, int stage_buf,
+                                     void* stream);
+
+/* oomb_grad_writeback: write every staged dK/dV block of `sel` (buffer stage_buf)
+ * back to its block of the host pools and set its grad_state to 1.  Must run after this chunk's backward and
+ * before any later oomb_grad_prefetch that reads those pages (one side stream
+ * keeps that order) and before buffer stage_buf is filled again.
+ * Errors: those of oomb_grad_prefetch. */
+OOMB_API oomb_status oomb_grad_writeback(oomb_pool* pool, const int32_t* sel, const int32_t* sel_count, int max_sel,
+                                         int stage_buf, void* stream);
+
+/* Offload mode: staging buffer that following attention calls read (K/V, and
+ * with offload_grads the dK/dV blocks the backward adds into). */
 OOMB_API oomb_status oomb_pool_set_stage(oomb_pool* pool, int stage_buf);
 
 /* Bytes of device workspace `op` needs for a chunk of n_q queries (0 on error). */

@@ -35,7 +35,8 @@ class PoolDesc(C.Structure):
         ("k_pool", C.c_void_p), ("v_pool", C.c_void_p), ("dk_pool", C.c_void_p), ("dv_pool", C.c_void_p),
         ("summary", C.c_void_p), ("page_table", C.c_void_p), ("error_word", C.c_void_p),
         ("page_order", C.c_void_p), ("offload", C.c_int), ("stage_k", C.c_void_p), ("stage_v", C.c_void_p),
-        ("stage_max_sel", C.c_int),
+        ("stage_max_sel", C.c_int), ("offload_grads", C.c_int), ("stage_dk", C.c_void_p),
+        ("stage_dv", C.c_void_p), ("grad_state", C.c_void_p),
     ]
 
 
@@ -67,6 +68,9 @@ def load(path: str = LIB_PATH) -> C.CDLL:
         "oomb_chunk_attn_bwd": (i32, [vp, vp, vp, vp, vp, i64, i32, vp, vp, i32, f32, vp, vp, sz, vp]),
         "oomb_prefetch": (i32, [vp, vp, vp, i32, i32, vp]),
         "oomb_pool_set_stage": (i32, [vp, i32]),
+        "oomb_grad_prefetch": (i32, [vp, vp, vp, i32, vp, vp, i32, vp]),
+        "oomb_grad_carry": (i32, [vp, vp, vp, i32, vp, vp, i32, vp]),
+        "oomb_grad_writeback": (i32, [vp, vp, vp, i32, i32, vp]),
         "oomb_workspace_size": (sz, [vp, i32, i32]),
         "oomb_check": (i32, [vp, vp, C.POINTER(C.c_uint32)]),
         "oomb_page_table_host": (i32, [vp, vp, i32]),
@@ -168,6 +172,22 @@ def oomb_chunk_attn_bwd(pool: int, q, o, d_o, lse, q_start: int, sel, sel_count,
 def oomb_prefetch(pool: int, sel, sel_count, stage_buf: int, stream=None) -> None:
     _ok("oomb_prefetch", load().oomb_prefetch(pool, _ptr(sel), _ptr(sel_count), sel.shape[-1], stage_buf,
                                               _stream(stream)))
+
+
+def oomb_grad_prefetch(pool: int, sel, sel_count, prev_sel, prev_count, stage_buf: int, stream=None) -> None:
+    _ok("oomb_grad_prefetch", load().oomb_grad_prefetch(pool, _ptr(sel), _ptr(sel_count), sel.shape[-1],
+                                                        _ptr(prev_sel), _ptr(prev_count), stage_buf,
+                                                        _stream(stream)))
+
+
+def oomb_grad_carry(pool: int, sel, sel_count, prev_sel, prev_count, stage_buf: int, stream=None) -> None:
+    _ok("oomb_grad_carry", load().oomb_grad_carry(pool, _ptr(sel), _ptr(sel_count), sel.shape[-1], _ptr(prev_sel),
+                                                  _ptr(prev_count), stage_buf, _stream(stream)))
+
+
+def oomb_grad_writeback(pool: int, sel, sel_count, stage_buf: int, stream=None) -> None:
+    _ok("oomb_grad_writeback", load().oomb_grad_writeback(pool, _ptr(sel), _ptr(sel_count), sel.shape[-1],
+                                                          stage_buf, _stream(stream)))
 
 
 def oomb_pool_set_stage(pool: int, stage_buf: int) -> None:

@@ -55,7 +55,7 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) fwd_rows(AttnArgs a) {
 
   const T* kp = reinterpret_cast<const T*>(a.kv.k);
   const T* vp = reinterpret_cast<const T*>(a.kv.v);
-  const int count = a.sel_count[h];
+  const int count = sel_count_checked(a, h);
   const int nvis = pages_visible(a);
   for (int s = 0; s < count; ++s) {
     bool ok = true;
@@ -165,7 +165,7 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32) bwd_dq_rows(AttnArgs a, co
 
   const T* kp = reinterpret_cast<const T*>(a.kv.k);
   const T* vp = reinterpret_cast<const T*>(a.kv.v);
-  const int count = a.sel_count[h];
+  const int count = sel_count_checked(a, h);
   const int nvis = pages_visible(a);
   for (int s = 0; s < count; ++s) {
     bool ok = true;
@@ -229,7 +229,7 @@ __global__ void __launch_bounds__(kDkdvThreads) bwd_dkdv(AttnArgs a, const float
   const int d = a.g.d, P = a.g.P, G = a.g.G;
   const int s = blockIdx.x, h = blockIdx.y, kt0 = blockIdx.z * kKT;
   if (kt0 >= P) return;
-  if (s >= a.sel_count[h]) return;
+  if (s >= sel_count_checked(a, h)) return;
   bool ok = true;
   const int nvis = pages_visible(a);
   const int p = sel_page(a, h, s, nvis, ok);
@@ -339,7 +339,7 @@ __global__ void __launch_bounds__(kDkdvThreads) bwd_dkdv(AttnArgs a, const float
     }
   }
   if (j >= kt) return;
-  const size_t gbase = (((size_t)phys * a.g.Hkv + h) * P + kt0 + j) * d;
+  const size_t gbase = (grad_block(a, h, s, phys) * P + kt0 + j) * d;
 #pragma unroll
   for (int c = 0; c < kColsPerThread; ++c) {
     const int col = cg + kColGroups * c;

@@ -6,14 +6,14 @@
 //
 // Kernels of one backward call:
 //   bwd_prep     D_i = dO_i . O_i (fp32) and zero the fp32 dQ accumulator
-//   bwd_main     n_split CTAs per (selected page, KV head), launched page-major
-//                (all KV heads of a page, then the next page; the chunk's own pages,
-//                which see fewer query tiles, last): K and V of the page stay in
-//                shared memory; the page's steps (every 128-row query tile that can
-//                see the page, for each of the G query heads of the group) are cut
-//                into n_split contiguous ranges, one per CTA, chosen on the host
-//                from a model of how the CTAs fill the SMs.  A CTA walks its steps
-//                in two 64-row halves:
+//   bwd_main     one thread-block cluster of n_split CTAs per (selected page, KV
+//                head), launched page-major (all KV heads of a page, then the next
+//                page; the chunk's own pages, which see fewer query tiles, last): K
+//                and V of the page stay in shared memory; the page's steps (every
+//                128-row query tile that can see the page, for each of the G query
+//                heads of the group) are cut into n_split contiguous ranges, one per
+//                CTA, chosen on the host from a model of how the clusters fill the
+//                SMs.  A CTA walks its steps in two 64-row halves:
 //                  S^T  = K Q_h^T       dP^T = V dO_h^T          (TMEM, fp32)
 //                  P^T  = exp2(S^T scale log2e - LSE log2e)     (masked on the diagonal)
 //                  dS^T = P^T (dP^T - D)
@@ -21,16 +21,20 @@
 //                  dQ^T = K^T dS^T      (dS^T also written to shared memory as the B
 //                                        operand; dQ^T read out of TMEM and added
 //                                        to the fp32 accumulator with global reductions)
-//                and finally adds scale*dK and dV into the page's rows of the fp32
-//                gradient pool with 16-byte float reductions (the n_split CTAs of a
-//                page share the rows; a sole owner reads, adds and writes).
+//                Epilogue: every CTA stages its partial dV | scale*dK in its own shared
+//                memory; CTA r of the cluster then owns key rows [128r/n, 128(r+1)/n):
+//                it sums the n partials of those rows in rank order, reading its
+//                peers' staging through distributed shared memory, and adds the sum
+//                into the page's rows of the fp32 gradient pool.  Every pool row has
+//                one writer and a fixed summation order: no atomics on the pool, and
+//                dK/dV are the same bits on every run.
 //   bwd_convert  dq = bf16(scale * dQ accumulator), token-major.
 //
 // Warp roles of bwd_main (448 threads):
 //   warp 0      TMA producer (K, V once; then a ring of Q/dO half tiles + LSE/D)
 //   warp 1      TMEM owner and MMA issuer
 //   warps 2-9   softmax: two warps per TMEM lane quarter (thread == key row), each
-//               owning 32 of the half tile's 64 query columns; epilogue for dK/dV
+//               owning 32 of the half tile's 64 query columns; the dK/dV epilogue
 //   warps 10-13 dQ read-out: thread == head-dim column (TMEM lane of dQ^T)
 // TMEM columns: half a [0,128), half b [128,256): S^T [0,64) dP^T [64,128); after the
 // softmax, query columns [32c, 32c+32) hold P^T packed in [32c, 32c+16) and dS^T
@@ -54,6 +58,8 @@ constexpr uint32_t kHalfTile = kHalf * kD * 2;  // 16 KB: one 64-row half tile (
 constexpr uint32_t kHalfBox = kHalfTile / 2;
 constexpr int kThreads = 448;
 constexpr int kSoftmaxThreads = 256;
+constexpr int kMaxCluster = 4;  // CTAs sharing one (page, KV head)
+constexpr int kBatch = 4;       // epilogue: pool rows in flight per thread
 
 struct BwdParams {
   const int32_t* sel;
@@ -62,14 +68,14 @@ struct BwdParams {
   const float* lse2;  // [Hq, n_pad] LSE * log2(e), +inf on padded rows
   const float* Dbuf;  // [Hq, n_pad] rowsum(dO * O), 0 on padded rows
   float* dq_acc;
-  float* dk_pool;
+  float* dk_pool;     // gradient pool, or the gradient staging buffers (grad_staged)
   float* dv_pool;
   uint32_t* err;
   int max_sel, n_q, n_pad, Hq, G, Hkv, num_phys, max_logical, n_tiles;
-  int n_split;  // CTAs sharing one (page, KV head): each takes a contiguous range of its steps
+  int n_split;  // CTAs (one cluster) sharing one (page, KV head): each takes a contiguous range of its steps
   int64_t q_start;
   float scale, scale_log2;
-  int staged, stage_h0, stage_stride;
+  int staged, stage_h0, stage_stride, grad_staged;
 };
 
 struct __align__(8) BwdBarriers {
@@ -81,6 +87,8 @@ struct __align__(8) BwdBarriers {
   uint64_t dq_full[2];
   uint64_t dq_free[2];
   uint64_t acc_full;
+  uint64_t staged;   // one arrival per CTA of the cluster: its partial dK/dV is staged
+  uint64_t reduced;  // one arrival per CTA of the cluster: it has read every staging
   uint32_t tmem_base;
   int abort;
 };
@@ -93,36 +101,56 @@ constexpr uint32_t kOffDS = kOffRing + kRing * 2 * kHalfTile;     // 2 x dS^T ha
 constexpr uint32_t kOffVec = kOffDS + 2 * kHalfTile;              // kRing x (lse2[64], D[64])
 constexpr uint32_t kOffBar = kOffVec + kRing * 2 * kHalf * 4;
 constexpr size_t kSmemBytes = 1024 + kOffBar + sizeof(BwdBarriers);
+// Epilogue staging of a CTA's partial gradients, over the K/V tiles and the ring (all
+// MMAs have completed by then): [128 key rows][64 float4] = dV columns (float4 0..31)
+// then scale*dK (32..63), float4 c of row j stored at position c ^ (j & 7).
+constexpr uint32_t kOffStage = 0;
+constexpr uint32_t kStageRow = 2 * kD * 4;  // 1 KB
+static_assert(kOffStage + kTile * kStageRow <= kOffDS, "staging must not reach the dS tiles");
+
+__device__ __forceinline__ uint32_t stage_off(int j, int c) {
+  return (uint32_t)j * kStageRow + (uint32_t)((c ^ (j & 7)) * 16);
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
                        const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                        const BwdParams p) {
-  // page-major order: every KV head of selected page s (and each of its n_split
-  // parts) before page s + 1, so that the lighter own pages run last
-  const int h = (int)(blockIdx.x % (unsigned)p.Hkv);
-  const int r = (int)(blockIdx.x / (unsigned)p.Hkv);
-  const int part = r % p.n_split, s = r / p.n_split;
-  if (s >= p.sel_count[h]) return;
+  // cluster = the n_split CTAs of one (page s, KV head h); page-major order: every KV
+  // head of selected page s before page s + 1, so that the lighter own pages run last.
+  // Every early return below depends on (s, h) alone, so a cluster leaves as a whole.
+  const int part = (int)(blockIdx.x % (unsigned)p.n_split);
+  const int r = (int)(blockIdx.x / (unsigned)p.n_split);
+  const int h = r % p.Hkv, s = r / p.Hkv;
+  const int32_t* row = p.sel + (size_t)h * p.max_sel;
+  int count = p.sel_count[h];
+  if (count < 0 || count > p.max_sel) {
+    if (threadIdx.x == 0 && part == 0 && s == 0) atomicOr(p.err, OOMB_DEVERR_SEL);
+    count = count < 0 ? 0 : p.max_sel;
+  }
+  if (s >= count) return;
   const int first_own = (int)(p.q_start / kTile);
   const int nvis = (int)((p.q_start + p.n_q + kTile - 1) / kTile);
-  const int pg = p.sel[(size_t)h * p.max_sel + s];
-  if (pg < 0 || pg >= nvis || pg >= p.max_logical) {
-    if (threadIdx.x == 0) atomicOr(p.err, OOMB_DEVERR_SEL);
+  const int pg = row[s];
+  // in range, and strictly above the previous entry and below the next one (so the
+  // whole selection is strictly ascending, the order the forward relies on)
+  if (pg < 0 || pg >= nvis || pg >= p.max_logical || (s > 0 && row[s - 1] >= pg) ||
+      (s + 1 < count && row[s + 1] <= pg)) {
+    if (threadIdx.x == 0 && part == 0) atomicOr(p.err, OOMB_DEVERR_SEL);
     return;
   }
   const int phys = p.table[pg];
   if (phys < 0 || phys >= p.num_phys) {
-    if (threadIdx.x == 0) atomicOr(p.err, OOMB_DEVERR_PAGE);
+    if (threadIdx.x == 0 && part == 0) atomicOr(p.err, OOMB_DEVERR_PAGE);
     return;
   }
   const int own = pg - first_own;           // >= 0 for the chunk's own pages
   const int t0 = own > 0 ? own : 0;
-  // steps (query tile t0 + su / G, query head su % G) for su in [u0, u0 + n_steps)
+  // steps (query tile t0 + su / G, query head su % G) for su in [u0, u0 + n_steps); a CTA
+  // with no step (fewer steps than CTAs) still stages a zero partial for the reduction
   const int all_steps = (p.n_tiles - t0) * p.G;
   const int u0 = (int)((int64_t)all_steps * part / p.n_split);
   const int n_steps = (int)((int64_t)all_steps * (part + 1) / p.n_split) - u0;
-  if (n_steps <= 0) return;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -144,6 +172,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar->dq_free[i], 4);                    // one arrival per read-out warp
     }
     mbar_init(&bar->acc_full, 1);
+    mbar_init(&bar->staged, (uint32_t)p.n_split);
+    mbar_init(&bar->reduced, (uint32_t)p.n_split);
     bar->abort = 0;
     fence_mbar_init();
   }
@@ -154,9 +184,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // every CTA of the cluster has initialised its barriers once all have arrived here;
+  // the epilogue waits for that before its first arrival on a peer's barrier
+  cluster_arrive();
   const uint32_t tmem = bar->tmem_base;
+  bool ok_acc = n_steps > 0;  // softmax warps: this CTA's dK/dV accumulators are complete
 
-  if (warp == 0) {
+  if (n_steps <= 0) {
+    // no step: nothing to load or compute
+  } else if (warp == 0) {
     // ------------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&tq);
@@ -318,46 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&bar->p_full[hh]);
       }
     }
-    // epilogue: this CTA's rows of the gradient pool += scale * dK, dV (64 columns per thread)
-    if (__all_sync(0xffffffffu, ok && mbar_wait(&bar->acc_full, 0, p.err, abort))) {
-      tc_fence_after();
-      const size_t row = (((size_t)phys * p.Hkv + h) * kTile + j) * kD + 64 * hc;
-      float4* gdv = reinterpret_cast<float4*>(p.dv_pool + row);
-      float4* gdk = reinterpret_cast<float4*>(p.dk_pool + row);
-#pragma unroll 1
-      for (int cc = 0; cc < 2; ++cc) {
-        uint32_t a[32], b[32];
-        tmem_ld32(tmem + lane_off + 256 + 64 * hc + cc * 32, a);
-        tmem_ld32(tmem + lane_off + 384 + 64 * hc + cc * 32, b);
-        tmem_wait_ld();
-        if (p.n_split > 1) {  // several CTAs add into these rows: 16-byte reductions
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            atomicAdd(gdv + cc * 8 + e, make_float4(__uint_as_float(a[4 * e]), __uint_as_float(a[4 * e + 1]),
-                                                    __uint_as_float(a[4 * e + 2]), __uint_as_float(a[4 * e + 3])));
-            atomicAdd(gdk + cc * 8 + e,
-                      make_float4(p.scale * __uint_as_float(b[4 * e]), p.scale * __uint_as_float(b[4 * e + 1]),
-                                  p.scale * __uint_as_float(b[4 * e + 2]), p.scale * __uint_as_float(b[4 * e + 3])));
-          }
-        } else {  // sole owner of the rows: read, add, write
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            float4 x = gdv[cc * 8 + e];
-            x.x += __uint_as_float(a[4 * e]);
-            x.y += __uint_as_float(a[4 * e + 1]);
-            x.z += __uint_as_float(a[4 * e + 2]);
-            x.w += __uint_as_float(a[4 * e + 3]);
-            gdv[cc * 8 + e] = x;
-            float4 y = gdk[cc * 8 + e];
-            y.x += p.scale * __uint_as_float(b[4 * e]);
-            y.y += p.scale * __uint_as_float(b[4 * e + 1]);
-            y.z += p.scale * __uint_as_float(b[4 * e + 2]);
-            y.w += p.scale * __uint_as_float(b[4 * e + 3]);
-            gdk[cc * 8 + e] = y;
-          }
-        }
-      }
-    }
+    ok_acc = ok;
   } else {
     // ------------------------------------------------------------------ dQ read-out
     // Each thread holds one head-dim column of dQ^T for the half's 64 query rows and adds
@@ -388,6 +385,105 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (rr < nrows) atomicAdd(dst + (size_t)rr * kD, __uint_as_float(r[rr]));
       }
     }
+  }
+
+  // ------------------------------------------------------------------ dK/dV epilogue
+  if (warp >= 2 && warp < 10) {
+    const int et = threadIdx.x - 64;  // 0..255
+    const int j = (warp & 3) * 32 + lane;  // key row == TMEM lane
+    const int hc = (warp - 2) >> 2;        // dV / dK columns [64 hc, 64 hc + 64)
+    const uint32_t lane_off = tmem_lane_base(warp);
+    // the pool rows this CTA will own: key rows [r0, r1) of the block's dV and dK, pulled
+    // into L2 while the partials are staged
+    const uint32_t n = (uint32_t)p.n_split;
+    const int rank = (int)cluster_ctarank();
+    const int r0 = kTile * rank / (int)n, r1 = kTile * (rank + 1) / (int)n;
+    const size_t blk = p.grad_staged ? (size_t)(p.stage_h0 + h) * p.stage_stride + s : (size_t)phys * p.Hkv + h;
+    float4* gdv = reinterpret_cast<float4*>(p.dv_pool + blk * kTile * kD);
+    float4* gdk = reinterpret_cast<float4*>(p.dk_pool + blk * kTile * kD);
+    if (et == 0) {
+      prefetch_l2(gdv + (size_t)r0 * (kD / 4), (uint32_t)(r1 - r0) * kD * 4);
+      prefetch_l2(gdk + (size_t)r0 * (kD / 4), (uint32_t)(r1 - r0) * kD * 4);
+    }
+    // (1) stage this CTA's partial (zero when it had no step or its pipeline gave up)
+    const bool have = __all_sync(0xffffffffu, ok_acc && mbar_wait(&bar->acc_full, 0, p.err, abort));
+    if (have) tc_fence_after();
+#pragma unroll 1
+    for (int cc = 0; cc < 2; ++cc) {
+      uint32_t a[32], b[32];
+      if (have) {
+        tmem_ld32(tmem + lane_off + 256 + 64 * hc + cc * 32, a);
+        tmem_ld32(tmem + lane_off + 384 + 64 * hc + cc * 32, b);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) a[e] = b[e] = 0u;
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int c = 16 * hc + 8 * cc + e;  // float4 column of dV; 32 + c of dK
+        *reinterpret_cast<float4*>(sm + kOffStage + stage_off(j, c)) =
+            make_float4(__uint_as_float(a[4 * e]), __uint_as_float(a[4 * e + 1]), __uint_as_float(a[4 * e + 2]),
+                        __uint_as_float(a[4 * e + 3]));
+        *reinterpret_cast<float4*>(sm + kOffStage + stage_off(j, 32 + c)) =
+            make_float4(p.scale * __uint_as_float(b[4 * e]), p.scale * __uint_as_float(b[4 * e + 1]),
+                        p.scale * __uint_as_float(b[4 * e + 2]), p.scale * __uint_as_float(b[4 * e + 3]));
+      }
+    }
+    fence_acq_rel_cluster();
+    named_bar_sync(1, kSoftmaxThreads);
+    cluster_wait();  // every peer's barriers are initialised
+    if (et == 0)
+      for (uint32_t q = 0; q < n; ++q) mbar_arrive_cluster(mapa_shared(smem_u32(&bar->staged), q));
+    // (2) reduce key rows [r0, r1) over the cluster's partials, in rank order, into the pool
+    if (__all_sync(0xffffffffu, mbar_wait_cluster(&bar->staged, 0, p.err))) {
+      const uint32_t base = smem_u32(sm + kOffStage);
+      const int n_items = (r1 - r0) * 64;  // (row, float4 column); a warp: one row, 32 consecutive float4
+      // kBatch items per thread in flight: pool loads (from L2, prefetched above) and the
+      // partials of every rank are all issued before the first add
+      for (int i0 = et; i0 < n_items; i0 += kBatch * kSoftmaxThreads) {
+        float4 x[kBatch], t[kBatch];
+        float4* g[kBatch];
+        uint32_t off[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int idx = min(i0 + u * kSoftmaxThreads, n_items - 1);  // clamped duplicates are not stored
+          const int jj = r0 + idx / 64, c = idx % 64;
+          off[u] = stage_off(jj, c);
+          g[u] = (c < 32 ? gdv : gdk) + (size_t)jj * (kD / 4) + (c & 31);
+          x[u] = *g[u];
+          t[u] = ld_dsmem_f4(mapa_shared(base + off[u], 0));
+        }
+        for (uint32_t q = 1; q < n; ++q) {
+#pragma unroll
+          for (int u = 0; u < kBatch; ++u) {
+            const float4 v = ld_dsmem_f4(mapa_shared(base + off[u], q));
+            t[u].x += v.x;
+            t[u].y += v.y;
+            t[u].z += v.z;
+            t[u].w += v.w;
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          if (i0 + u * kSoftmaxThreads < n_items) {
+            x[u].x += t[u].x;
+            x[u].y += t[u].y;
+            x[u].z += t[u].z;
+            x[u].w += t[u].w;
+            *g[u] = x[u];
+          }
+        }
+      }
+    }
+    // (3) this CTA has read every peer's staging; wait until its own was read by all
+    fence_acq_rel_cluster();
+    named_bar_sync(1, kSoftmaxThreads);
+    if (et == 0)
+      for (uint32_t q = 0; q < n; ++q) mbar_arrive_cluster(mapa_shared(smem_u32(&bar->reduced), q));
+    mbar_wait_cluster(&bar->reduced, 0, p.err);
+  } else {
+    cluster_wait();  // every thread that arrived also waits once (long complete by now)
   }
   tc_fence_before();
   __syncthreads();
@@ -446,29 +542,32 @@ __global__ void bwd_convert(const float* __restrict__ dq_acc, int n_q, int Hq, f
   *reinterpret_cast<uint2*>(dq + ((size_t)i * Hq + hq) * kD + lane * 4) = out;
 }
 
-}  // namespace
-
-// How many CTAs share one (page, KV head).  A CTA's work is its number of steps
-// (query tile x query head); history pages have n_tiles * G of them and the chunk's
-// own page k has (n_tiles - k) * G.  With one CTA per SM, CTAs start in launch order
-// on the first SM that frees up; that greedy schedule is replayed here for
-// kMinSplit..kMaxSplit parts, each CTA also paying a fixed cost (K/V load, pipeline
-// fill and drain, the dK/dV epilogue) of about one step, and the fewest parts within
-// 1% of the shortest schedule win.  Measured on GB300 (backward calls of whole
-// sweeps), two parts beat one on every workload, also where this model sees no
-// tail (1M tokens, chunks of 8192: 923 against 906 TFLOP/s), so two is the floor;
-// three win where the grid is small (a 4K-token window over 4K chunks: 857 against
-// 838 with two, 671 with one).  The selection counts live on the device, so every
-// one of the max_sel slots is assumed filled; empty slots exit at once.  Cached per
-// shape.
+// How many CTAs (one cluster) share one (page, KV head).  A CTA's work is its number of
+// steps (query tile x query head); history pages have n_tiles * G of them and the
+// chunk's own page k has (n_tiles - k) * G.  A cluster of ns CTAs splits a page's steps
+// into ns ranges and starts as a whole once ns SMs are free: with cluster_slots[ns]
+// clusters resident at once (the device's cluster occupancy, which leaves SMs idle
+// where a GPC's SM count is not a multiple of ns), the clusters start in launch order
+// on the first free slot, each taking its longest part plus a fixed cost (K/V load,
+// pipeline fill and drain, the dK/dV reduction) of about one step.  That greedy
+// schedule is replayed for kMinSplit..kMaxSplit CTAs, and the fewest within 1% of the
+// shortest schedule win.  Measured on GB300 (backward calls of whole sweeps), two CTAs
+// beat one on every workload, also where this model sees no tail (1M tokens, chunks
+// of 8192: 923 against 906 TFLOP/s), so two is the floor; more win where the grid is
+// small (a 4K-token window over 4K chunks).  The selection counts live on the device,
+// so every one of the max_sel slots is assumed filled; empty slots exit at once.
+// Cached per shape.
 constexpr int kMinSplit = 2;
-constexpr int kMaxSplit = 4;
+constexpr int kMaxSplit = kMaxCluster;
 constexpr double kCtaOverheadSteps = 1.0;
 
-int bwd_split(int max_sel, int n_own, int n_tiles, int G, int Hkv, int n_sm) {
+}  // namespace
+
+int bwd_split(int max_sel, int n_own, int n_tiles, int G, int Hkv, const int* cluster_slots) {
   static std::mutex mu;
-  static std::map<std::array<int, 6>, int> cache;
-  const std::array<int, 6> key = {max_sel, n_own, n_tiles, G, Hkv, n_sm};
+  static std::map<std::array<int, 9>, int> cache;
+  const std::array<int, 9> key = {max_sel, n_own, n_tiles, G, Hkv, cluster_slots[1], cluster_slots[2],
+                                  cluster_slots[3], cluster_slots[4]};
   {
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(key);
@@ -476,26 +575,25 @@ int bwd_split(int max_sel, int n_own, int n_tiles, int G, int Hkv, int n_sm) {
   }
   const int n_hist = std::max(0, max_sel - n_own);
   int best = kMinSplit;
-  double best_t = 0.0;
+  double best_t = -1.0;
   for (int ns = kMinSplit; ns <= kMaxSplit; ++ns) {
+    const int slots = cluster_slots[ns];
+    if (slots <= 0) continue;
     std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
-    for (int i = 0; i < n_sm; ++i) free_at.push(0.0);
+    for (int i = 0; i < slots; ++i) free_at.push(0.0);
     double end = 0.0;
     for (int sl = 0; sl < max_sel; ++sl) {
       const int k = sl - n_hist;  // own page index (< 0: history page)
       const int steps = (n_tiles - (k > 0 ? k : 0)) * G;
-      for (int part = 0; part < ns; ++part) {
-        const int w = (int)((int64_t)steps * (part + 1) / ns - (int64_t)steps * part / ns);
-        if (w <= 0) continue;
-        for (int hk = 0; hk < Hkv; ++hk) {
-          const double t = free_at.top() + kCtaOverheadSteps + w;
-          free_at.pop();
-          free_at.push(t);
-          end = std::max(end, t);
-        }
+      const int w = (steps + ns - 1) / ns;  // longest part
+      for (int hk = 0; hk < Hkv; ++hk) {
+        const double t = free_at.top() + kCtaOverheadSteps + w;
+        free_at.pop();
+        free_at.push(t);
+        end = std::max(end, t);
       }
     }
-    if (ns == kMinSplit || end < 0.99 * best_t) {
+    if (best_t < 0.0 || end < 0.99 * best_t) {
       best = ns;
       best_t = end;
     }
@@ -504,6 +602,41 @@ int bwd_split(int max_sel, int n_own, int n_tiles, int G, int Hkv, int n_sm) {
   cache[key] = best;
   return best;
 }
+
+namespace {
+
+// Clusters of ns CTAs of the backward kernel that can be resident at once on the
+// current device (cudaOccupancyMaxActiveClusters), per device and ns.
+cudaError_t cluster_slots(int* out /* [kMaxSplit + 1] */) {
+  static int slots[kMaxDevices][kMaxSplit + 1] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (!slots[dev][1]) {
+    int tmp[kMaxSplit + 1] = {};
+    for (int ns = 1; ns <= kMaxSplit; ++ns) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(ns * 64);
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = kSmemBytes;
+      cudaLaunchAttribute attr;
+      attr.id = cudaLaunchAttributeClusterDimension;
+      attr.val.clusterDim.x = ns;
+      attr.val.clusterDim.y = 1;
+      attr.val.clusterDim.z = 1;
+      cfg.attrs = &attr;
+      cfg.numAttrs = 1;
+      e = cudaOccupancyMaxActiveClusters(&tmp[ns], (const void*)attn_bwd_tc_kernel, &cfg);
+      if (e != cudaSuccess) return e;
+    }
+    for (int ns = 1; ns <= kMaxSplit; ++ns) slots[dev][ns] = tmp[ns];
+  }
+  for (int ns = 0; ns <= kMaxSplit; ++ns) out[ns] = slots[dev][ns];
+  return cudaSuccess;
+}
+
+}  // namespace
 
 size_t bwd_tc_workspace_bytes(const Geometry& g, int n_q) {
   const size_t n_pad = (size_t)(n_q + kTile - 1) / kTile * kTile;
@@ -553,11 +686,27 @@ cudaError_t launch_attn_bwd_tc(const AttnArgs& a, cudaStream_t st) {
   p.staged = a.kv.staged;
   p.stage_h0 = a.kv.stage_h0;
   p.stage_stride = a.kv.stage_stride;
+  p.grad_staged = a.grad_staged;
   const int first_own = (int)(a.q_start / kTile);
   const int n_own = (int)((a.q_start + a.n_q + kTile - 1) / kTile) - first_own;
-  p.n_split = bwd_split(a.max_sel, n_own, p.n_tiles, p.G, p.Hkv, device_sm_count());
-  const unsigned grid = (unsigned)a.max_sel * (unsigned)p.n_split * (unsigned)p.Hkv;
-  attn_bwd_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(tq, tdo, tk, tv, p);
+  int slots[kMaxSplit + 1];
+  e = cluster_slots(slots);
+  if (e != cudaSuccess) return e;
+  p.n_split = bwd_split(a.max_sel, n_own, p.n_tiles, p.G, p.Hkv, slots);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)a.max_sel * (unsigned)p.n_split * (unsigned)p.Hkv);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = (unsigned)p.n_split;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, attn_bwd_tc_kernel, tq, tdo, tk, tv, p);
+  if (e != cudaSuccess) return e;
   bwd_convert<<<(warps + 7) / 8, 256, 0, st>>>(dq_acc, a.n_q, a.g.Hq, a.scale,
                                                reinterpret_cast<__nv_bfloat16*>(a.dq));
   count_launches(3);

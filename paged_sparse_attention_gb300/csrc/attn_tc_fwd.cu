@@ -104,7 +104,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool hasB = tB < p.n_tiles;
   const int h = hq / p.G;
   const int diagA = (int)(p.q_start / kTile) + tA;
-  const int count = p.sel_count[h];
+  int count = p.sel_count[h];
+  if (count < 0 || count > p.max_sel) {  // flagged by the producer below; never read past the row
+    count = count < 0 ? 0 : p.max_sel;
+  }
   const int nA = pages_upto(p, h, count, diagA);
   const int nB = hasB ? pages_upto(p, h, count, diagA + 1) : 0;
   const int n = max(nA, nB);  // pages loaded
@@ -144,14 +147,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tq);
       tma_prefetch_desc(&tk);
       tma_prefetch_desc(&tv);
-      // every selection entry must name an existing page of this chunk's view
+      // the selection must be strictly ascending pages of this chunk's view (the tiles
+      // take its prefixes); a count outside [0, max_sel] is flagged too
       const int nvis = (int)((p.q_start + p.n_q + kTile - 1) / kTile);
+      const int raw_count = p.sel_count[h];
+      if (raw_count < 0 || raw_count > p.max_sel) atomicOr(p.err, OOMB_DEVERR_SEL);
+      int prev = -1;
       for (int e = 0; e < count; ++e) {
         const int pe = p.sel[(size_t)h * p.max_sel + e];
-        if (pe < 0 || pe >= nvis) {
+        if (pe <= prev || pe >= nvis) {
           atomicOr(p.err, OOMB_DEVERR_SEL);
           break;
         }
+        prev = pe;
       }
       mbar_arrive_expect_tx(&bar->q_full, (hasB ? 2u : 1u) * kTileBytes);
       tma_load_3d(sm + kOffQ, &tq, &bar->q_full, 0, hq, tA * kTile);

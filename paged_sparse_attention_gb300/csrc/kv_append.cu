@@ -36,7 +36,8 @@ __global__ void __launch_bounds__(kAppendThreads)
     kv_append_kernel(Geometry g, T* __restrict__ k_pool, T* __restrict__ v_pool, float* __restrict__ dk_pool,
                      float* __restrict__ dv_pool, float* __restrict__ summary, int32_t* __restrict__ table,
                      const T* __restrict__ k, const T* __restrict__ v, int64_t first_token, int64_t end_token,
-                     int first_new_logical, const __grid_constant__ NewPages np, int n_new, uint32_t* err) {
+                     int first_new_logical, const __grid_constant__ NewPages np, int n_new, uint8_t* grad_state,
+                     uint32_t* err) {
   const int i = blockIdx.x, h = blockIdx.y;
   const int P = g.P, d = g.d, Hkv = g.Hkv;
   const int phys = np.phys[i];
@@ -85,13 +86,18 @@ __global__ void __launch_bounds__(kAppendThreads)
       }
     }
   }
-  // zero both gradient pages (streaming stores: they are next read by a later backward)
-  const int nvec4 = P * d / 4;
-  float4* gk = reinterpret_cast<float4*>(dk_pool + blk);
-  float4* gv = reinterpret_cast<float4*>(dv_pool + blk);
-  for (int idx = threadIdx.x; idx < nvec4; idx += kAppendThreads) {
-    __stcs(gk + idx, make_float4(0.f, 0.f, 0.f, 0.f));
-    __stcs(gv + idx, make_float4(0.f, 0.f, 0.f, 0.f));
+  if (grad_state) {
+    // gradient pools in host memory: the block counts as zero until its first write-back
+    if (threadIdx.x == 0) grad_state[(size_t)phys * Hkv + h] = 0;
+  } else {
+    // zero both gradient pages (streaming stores: they are next read by a later backward)
+    const int nvec4 = P * d / 4;
+    float4* gk = reinterpret_cast<float4*>(dk_pool + blk);
+    float4* gv = reinterpret_cast<float4*>(dv_pool + blk);
+    for (int idx = threadIdx.x; idx < nvec4; idx += kAppendThreads) {
+      __stcs(gk + idx, make_float4(0.f, 0.f, 0.f, 0.f));
+      __stcs(gv + idx, make_float4(0.f, 0.f, 0.f, 0.f));
+    }
   }
   // mean key over the m tokens present: fixed-order reduction, deterministic
   __shared__ float part[kAppendThreads * VEC];
@@ -111,7 +117,7 @@ __global__ void __launch_bounds__(kAppendThreads)
 cudaError_t launch_kv_append(const Geometry& g, void* k_pool, void* v_pool, float* dk_pool, float* dv_pool,
                              float* summary, int32_t* table, const void* k, const void* v, int64_t first_token,
                              int n_tokens, int64_t total_tokens, const int32_t* new_phys, int n_new,
-                             int first_new_logical, uint32_t* err, cudaStream_t st) {
+                             int first_new_logical, uint8_t* grad_state, uint32_t* err, cudaStream_t st) {
   (void)n_tokens;
   for (int base = 0; base < n_new; base += kMaxNewPerLaunch) {
     const int cnt = n_new - base < kMaxNewPerLaunch ? n_new - base : kMaxNewPerLaunch;
@@ -121,12 +127,12 @@ cudaError_t launch_kv_append(const Geometry& g, void* k_pool, void* v_pool, floa
     if (g.dtype == OOMB_FP32) {
       kv_append_kernel<float><<<grid, kAppendThreads, 0, st>>>(
           g, (float*)k_pool, (float*)v_pool, dk_pool, dv_pool, summary, table, (const float*)k, (const float*)v,
-          first_token, total_tokens, first_new_logical + base, np, cnt, err);
+          first_token, total_tokens, first_new_logical + base, np, cnt, grad_state, err);
     } else {
       kv_append_kernel<__nv_bfloat16><<<grid, kAppendThreads, 0, st>>>(
           g, (__nv_bfloat16*)k_pool, (__nv_bfloat16*)v_pool, dk_pool, dv_pool, summary, table,
           (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, first_token, total_tokens, first_new_logical + base,
-          np, cnt, err);
+          np, cnt, grad_state, err);
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;

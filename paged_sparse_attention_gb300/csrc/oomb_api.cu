@@ -157,6 +157,10 @@ oomb_status oomb_pool_create(const oomb_pool_desc* desc, oomb_pool** out) {
     if (!d.stage_k || !d.stage_v || d.stage_max_sel <= 0) return OOMB_ERR_ARG;
     if (!aligned(d.stage_k, 16) || !aligned(d.stage_v, 16)) return OOMB_ERR_ALIGN;
   }
+  if (d.offload_grads) {
+    if (!d.offload || !d.stage_dk || !d.stage_dv || !d.grad_state) return OOMB_ERR_ARG;
+    if (!aligned(d.stage_dk, 16) || !aligned(d.stage_dv, 16)) return OOMB_ERR_ALIGN;
+  }
   oomb_pool* p = new (std::nothrow) oomb_pool;
   if (!p) return OOMB_ERR_ARG;
   p->d = d;
@@ -230,7 +234,8 @@ oomb_status oomb_kv_append(oomb_pool* p, const void* k, const void* v, int64_t f
   }
   e = launch_kv_append(p->g, p->d.k_pool, p->d.v_pool, p->d.dk_pool, p->d.dv_pool, p->d.summary,
                                    p->d.page_table, k, v, first_token, n_tokens, end, newp.data(), n_new,
-                                   (int)first_page, p->d.error_word, (cudaStream_t)stream);
+                                   (int)first_page, p->d.offload_grads ? p->d.grad_state : nullptr,
+                                   p->d.error_word, (cudaStream_t)stream);
   if (e != cudaSuccess) {
     for (int i = n_new - 1; i >= 0; --i) {
       p->free_list.push_back(newp[i]);
@@ -320,8 +325,15 @@ static AttnArgs make_args(oomb_pool* p, const void* q, int64_t q_start, int n_q,
   a.max_sel = max_sel;
   a.scale = scale;
   a.err = p->d.error_word;
-  a.dk_pool = p->d.dk_pool;
-  a.dv_pool = p->d.dv_pool;
+  if (p->d.offload_grads) {  // the backward adds into the staged gradient blocks
+    a.dk_pool = p->d.stage_dk;
+    a.dv_pool = p->d.stage_dv;
+    a.grad_staged = 1;
+  } else {
+    a.dk_pool = p->d.dk_pool;
+    a.dv_pool = p->d.dv_pool;
+    a.grad_staged = 0;
+  }
   return a;
 }
 
@@ -372,6 +384,45 @@ oomb_status oomb_prefetch(oomb_pool* p, const int32_t* sel, const int32_t* sel_c
   return cuda_status(launch_prefetch(p->g, p->d.k_pool, p->d.v_pool, p->d.page_table, sel, sel_count, max_sel,
                                      p->d.stage_k, p->d.stage_v, stage_buf * p->g.Hkv, p->d.stage_max_sel,
                                      p->d.error_word, (cudaStream_t)stream));
+}
+
+// Shared checks of the gradient staging calls.
+static oomb_status check_grad_call(const oomb_pool* p, const int32_t* sel, const int32_t* sel_count, int max_sel,
+                                   int stage_buf) {
+  if (!p || !sel || !sel_count || max_sel <= 0) return OOMB_ERR_ARG;
+  if (!p->d.offload_grads) return OOMB_ERR_UNSUPPORTED;
+  if (stage_buf < 0 || stage_buf > 1 || max_sel > p->d.stage_max_sel) return OOMB_ERR_ARG;
+  if (!aligned(sel, 4) || !aligned(sel_count, 4)) return OOMB_ERR_ALIGN;
+  return OOMB_OK;
+}
+
+oomb_status oomb_grad_prefetch(oomb_pool* p, const int32_t* sel, const int32_t* sel_count, int max_sel,
+                               const int32_t* prev_sel, const int32_t* prev_count, int stage_buf, void* stream) {
+  oomb_status s = check_grad_call(p, sel, sel_count, max_sel, stage_buf);
+  if (s != OOMB_OK) return s;
+  if ((prev_sel == nullptr) != (prev_count == nullptr)) return OOMB_ERR_ARG;
+  return cuda_status(launch_grad_copy(p->g, kGradFromHost, p->d.dk_pool, p->d.dv_pool, p->d.grad_state, p->d.page_table, sel,
+                                      sel_count, prev_sel, prev_count, max_sel, p->d.stage_dk, p->d.stage_dv,
+                                      stage_buf, p->d.stage_max_sel, p->d.error_word, (cudaStream_t)stream));
+}
+
+oomb_status oomb_grad_carry(oomb_pool* p, const int32_t* sel, const int32_t* sel_count, int max_sel,
+                            const int32_t* prev_sel, const int32_t* prev_count, int stage_buf, void* stream) {
+  oomb_status s = check_grad_call(p, sel, sel_count, max_sel, stage_buf);
+  if (s != OOMB_OK) return s;
+  if (!prev_sel || !prev_count) return OOMB_ERR_ARG;
+  return cuda_status(launch_grad_copy(p->g, kGradCarry, p->d.dk_pool, p->d.dv_pool, p->d.grad_state, p->d.page_table, sel,
+                                      sel_count, prev_sel, prev_count, max_sel, p->d.stage_dk, p->d.stage_dv,
+                                      stage_buf, p->d.stage_max_sel, p->d.error_word, (cudaStream_t)stream));
+}
+
+oomb_status oomb_grad_writeback(oomb_pool* p, const int32_t* sel, const int32_t* sel_count, int max_sel,
+                                int stage_buf, void* stream) {
+  oomb_status s = check_grad_call(p, sel, sel_count, max_sel, stage_buf);
+  if (s != OOMB_OK) return s;
+  return cuda_status(launch_grad_copy(p->g, kGradToHost, p->d.dk_pool, p->d.dv_pool, p->d.grad_state, p->d.page_table, sel,
+                                      sel_count, nullptr, nullptr, max_sel, p->d.stage_dk, p->d.stage_dv, stage_buf,
+                                      p->d.stage_max_sel, p->d.error_word, (cudaStream_t)stream));
 }
 
 oomb_status oomb_pool_set_stage(oomb_pool* p, int stage_buf) {

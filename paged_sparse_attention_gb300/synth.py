@@ -42,6 +42,7 @@ class Workload:
     plant_beta: float = 1.0
     base_seed: int = 1000
     offload: bool = False
+    offload_grads: bool = False  # with offload: the fp32 dK/dV pools live in pinned host memory too
     window: int = -1      # >= 0: local sliding-window selection of this many history pages (no top-K)
 
     @property
@@ -90,9 +91,10 @@ WORKLOADS: Dict[str, Workload] = {
     # 1M tokens in chunks of 8192, top-128 pages.
     "sparse1m": Workload("sparse1m", 28, 4, 128, "bf16", 1048576, 8192, 128, 128,
                          rope=True, plants=8, base_seed=1003),
-    # 4M tokens, KV pages in pinned host memory, selected pages prefetched to HBM.
+    # 4M tokens, KV pages and their fp32 gradient pages in pinned host memory; the
+    # selected blocks are staged in HBM on a side stream.
     "offload4m": Workload("offload4m", 28, 4, 128, "bf16", 4194304, 8192, 128, 128,
-                          rope=True, plants=8, base_seed=1004, offload=True),
+                          rope=True, plants=8, base_seed=1004, offload=True, offload_grads=True),
     # 128K tokens with local sliding-window attention (the sparse layers of a
     # sparse-native model): the 32 pages (4K tokens) before each 4K chunk plus the
     # chunk's own pages, no sink and no top-K.

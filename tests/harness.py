@@ -51,7 +51,7 @@ class GpuSweep:
     the staging buffer of its parity before its attention calls."""
 
     def __init__(self, w: synth.Workload, chunks, order, dev="cuda", sel_override=None, scale=None,
-                 num_phys: Optional[int] = None, offload: bool = False):
+                 num_phys: Optional[int] = None, offload: bool = False, offload_grads: bool = False):
         self.w = w
         self.dev = torch.device(dev)
         self.scale = 1.0 / math.sqrt(w.head_dim) if scale is None else scale
@@ -61,8 +61,9 @@ class GpuSweep:
         self.max_sel = max_sel
         self.pool = PagedKVPool(w.n_q_heads, w.n_kv_heads, w.head_dim, w.page, n_phys, w.n_pages,
                                 w.torch_dtype, self.dev, page_order=torch.as_tensor(order, dtype=torch.int32),
-                                offload=offload, stage_max_sel=max_sel if offload else 0)
-        side = torch.cuda.Stream(device=self.dev) if offload else None
+                                offload=offload, stage_max_sel=max_sel if offload else 0,
+                                offload_grads=offload_grads)
+        side = torch.cuda.Stream(device=self.dev, priority=-1) if offload else None
         main = torch.cuda.current_stream(self.dev)
 
         def stage(c, sel, cnt):
@@ -104,14 +105,27 @@ class GpuSweep:
             start, n = w.chunk_bounds(c)
             g = dev_chunks[c]
             stage(c, g["sel"], g["cnt"])
+            if offload_grads:  # dK/dV blocks of the selection: from the host, or carried from chunk c + 1
+                prev = dev_chunks[c + 1] if c + 1 < len(chunks) else None
+                with torch.cuda.stream(side):
+                    L.oomb_grad_prefetch(h, g["sel"], g["cnt"], prev["sel"] if prev else None,
+                                         prev["cnt"] if prev else None, c % 2, stream=side)
+                    if prev is not None:
+                        L.oomb_grad_carry(h, g["sel"], g["cnt"], prev["sel"], prev["cnt"], c % 2, stream=side)
+                main.wait_stream(side)
             o = torch.empty_like(g["q"])
             lse = torch.empty(w.n_q_heads, n, dtype=torch.float32, device=self.dev)
             L.oomb_chunk_attn_fwd(h, g["q"], start, g["sel"], g["cnt"], self.scale, o, lse)  # recompute
             dq = torch.empty_like(g["q"])
             L.oomb_chunk_attn_bwd(h, g["q"], o, g["do"], lse, start, g["sel"], g["cnt"], self.scale, dq, ws_bwd)
+            if offload_grads:  # staged dK/dV back to the host pools
+                side.wait_stream(main)
+                L.oomb_grad_writeback(h, g["sel"], g["cnt"], c % 2, stream=side)
             self.dQ[c] = dq
             self.O2.insert(0, o)
             self.LSE2.insert(0, lse)
+        if offload:
+            main.wait_stream(side)
         self.err_bits = L.oomb_check(h)
         self.dK, self.dV = self.pool.logical_grads(w.seq)
 

@@ -93,5 +93,12 @@ def test_algorithmic_bytes_per_call():
     # the summary row of a page is shared by its P tokens: d * 4 / P bytes per token and head
     assert st["device"] == 10_000 * Hkv * d * (2 * 2 + 2 * 4) + 10_000 * Hkv * d * 4 // P
     assert st["host"] == 0
-    off = bench.state_bytes_per_10k(synth.WORKLOADS["offload4m"])  # K/V move to pinned host memory
-    assert off["host"] == 10_000 * Hkv * d * 2 * 2 and off["device"] == st["device"] - off["host"]
+    w4 = synth.WORKLOADS["offload4m"]
+    # K/V (bf16) and dK/dV (fp32) move to pinned host memory: only the summaries grow on the device
+    off = bench.state_bytes_per_10k(synth.WORKLOADS["offload4m"])
+    assert off["host"] == 10_000 * Hkv * d * (2 * 2 + 2 * 4) and off["device"] == st["device"] - off["host"]
+    assert off["device"] == 10_000 * Hkv * d * 4 // P
+    # fixed staging: two buffers of max_sel blocks per KV head, K/V bf16 and dK/dV fp32
+    assert off["fixed_staging_device"] == 2 * Hkv * w4.max_sel * P * d * (2 * 2 + 2 * 4)
+    kv_only = bench.state_bytes_per_10k(synth.scaled(w4, "kv_only", offload_grads=False))
+    assert kv_only["host"] == 10_000 * Hkv * d * 2 * 2 and kv_only["device"] == st["device"] - kv_only["host"]

@@ -16,7 +16,7 @@ import paged_sparse_attention_gb300 as L
 from paged_sparse_attention_gb300 import synth
 from paged_sparse_attention_gb300.pool import PagedKVPool
 
-from harness import TOL, GpuSweep, f64, make_chunks, oracle_sweep
+from harness import TOL, GpuSweep, f64, make_chunks, oracle_sweep, pad_sel
 
 pytestmark = pytest.mark.gpu
 
@@ -196,29 +196,102 @@ def test_host_errors_on_gpu():
     pool.close()
 
 
+@pytest.mark.parametrize("grads", [False, True], ids=["kv", "kv+grads"])
 @pytest.mark.parametrize("name", ["bf16_sparse", "fp32_sparse", "bf16_window"])
-def test_offload_matches_resident(name):
-    """K/V pools in pinned host memory, selected pages prefetched on a side stream:
-    same outputs as the HBM-resident run (bitwise for O and LSE; dQ, and dK/dV of
-    pages whose backward is split over several thread blocks, are summed with float
-    reductions in a run-dependent order), and within tolerance of the oracle."""
+def test_offload_matches_resident(name, grads):
+    """K/V pools (and with grads the fp32 dK/dV pools) in pinned host memory, the
+    selected blocks staged in HBM on a side stream (gradients staged in from the host
+    or carried over from the previous chunk, and written back after each backward):
+    the same outputs as the HBM-resident run -- bitwise for O, LSE, dK and dV (each
+    gradient row is summed in a fixed order), dQ to rounding (fp32 reductions across
+    thread blocks in a run-dependent order) -- and within tolerance of the oracle."""
     w = {**CASES, **WINDOW_CASES}[name]
     chunks, _ = make_chunks(w)
     order = synth.page_order(w).tolist()
     ref = oracle_sweep(w, chunks, order)
     res = GpuSweep(w, chunks, order, sel_override=ref["sel"])
-    off = GpuSweep(w, chunks, order, sel_override=ref["sel"], offload=True)
+    off = GpuSweep(w, chunks, order, sel_override=ref["sel"], offload=True, offload_grads=grads)
     assert off.err_bits == 0
     for c in range(w.n_chunks):
         assert torch.equal(off.O[c], res.O[c]) and torch.equal(off.LSE[c], res.LSE[c])
         assert O.rel_l2(f64(off.dQ[c]), f64(res.dQ[c])) < 1e-3
         assert O.rel_l2(f64(off.dQ[c]), ref["dQ"][c]) < TOL[w.dtype]
-    assert O.rel_l2(f64(off.dK), f64(res.dK)) < 1e-6 and O.rel_l2(f64(off.dV), f64(res.dV)) < 1e-6
+    assert torch.equal(off.dK.cpu(), res.dK.cpu()) and torch.equal(off.dV.cpu(), res.dV.cpu())
+    rdk, rdv = ref["pool"].logical_grads()
+    assert O.rel_l2(f64(off.dK), rdk) < TOL[w.dtype] and O.rel_l2(f64(off.dV), rdv) < TOL[w.dtype]
     for a, b in zip(off.gpu_sel, res.gpu_sel):
         for x, y in zip(a, b):
             assert np.array_equal(x, y)
     res.pool.close()
     off.pool.close()
+
+
+@pytest.mark.parametrize("name", ["bf16_sparse", "bf16_dense"])
+def test_backward_gradients_deterministic(name):
+    """dK/dV are partitioned by (page, KV head): the thread blocks that share a block
+    sum their partials in a fixed order and add them once, so two runs of the same
+    sweep give bit-identical gradient pools (no float atomics on the pool)."""
+    w = CASES[name]
+    chunks, _ = make_chunks(w)
+    order = synth.page_order(w).tolist()
+    a = GpuSweep(w, chunks, order)
+    b = GpuSweep(w, chunks, order)
+    assert a.err_bits == 0 and b.err_bits == 0
+    assert torch.equal(a.dK, b.dK) and torch.equal(a.dV, b.dV)
+    for c in range(w.n_chunks):
+        assert torch.equal(a.O[c], b.O[c]) and torch.equal(a.LSE[c], b.LSE[c])
+    a.pool.close()
+    b.pool.close()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("bad", ["unsorted", "duplicate", "count_too_large", "negative_count"])
+def test_malformed_selection_is_flagged(dtype, bad):
+    """A selection that is not strictly ascending, repeats a page, or has a count
+    outside [0, max_sel] raises OOMB_DEVERR_SEL (status KERNEL from oomb_check) in the
+    forward and in the backward; the kernels read only inside the selection row, and
+    the context stays usable (a valid call afterwards is clean)."""
+    w = synth.scaled(QWEN, f"badsel_{dtype}", seq=1024, chunk=512, top_k=-1, plants=0, dtype=dtype)
+    if dtype == "fp32":
+        w = synth.scaled(synth.WORKLOADS["tiny"], "badsel_fp32", seq=512, chunk=256)
+    chunks, _ = make_chunks(w, plants=False)
+    dev = torch.device("cuda")
+    pool = PagedKVPool(w.n_q_heads, w.n_kv_heads, w.head_dim, w.page, w.num_phys, w.n_pages, w.torch_dtype,
+                       dev, page_order=synth.page_order(w))
+    for c, ch in enumerate(chunks):
+        L.oomb_kv_append(pool.handle, ch["k"].to(dev), ch["v"].to(dev), w.chunk_bounds(c)[0])
+    c = w.n_chunks - 1
+    start, n = w.chunk_bounds(c)
+    q, do = chunks[c]["q"].to(dev), chunks[c]["do"].to(dev)
+    n_vis = -(-(start + n) // w.page)
+    good = list(range(n_vis))
+    max_sel = n_vis + 2
+    rows = {"unsorted": [good[1], good[0]] + good[2:], "duplicate": good[:2] + [good[1]] + good[2:],
+            "count_too_large": good, "negative_count": good}[bad]
+    sel = torch.full((w.n_kv_heads, max_sel), -1, dtype=torch.int32)
+    sel[:, : len(rows)] = torch.tensor(rows, dtype=torch.int32)
+    count = {"count_too_large": max_sel + 5, "negative_count": -3}.get(bad, len(rows))
+    cnt = torch.full((w.n_kv_heads,), count, dtype=torch.int32)
+    sel, cnt = sel.to(dev), cnt.to(dev)
+    scale = 1.0 / math.sqrt(w.head_dim)
+    o = torch.empty_like(q)
+    lse = torch.empty(w.n_q_heads, n, dtype=torch.float32, device=dev)
+    L.oomb_chunk_attn_fwd(pool.handle, q, start, sel, cnt, scale, o, lse)
+    with pytest.raises(L.OombError) as e:
+        L.oomb_check(pool.handle)
+    assert e.value.status == 5
+    ws = pool.workspace(L.OOMB_OP_BWD, n)
+    dq = torch.empty_like(q)
+    L.oomb_chunk_attn_bwd(pool.handle, q, o, do, lse, start, sel, cnt, scale, dq, ws)
+    with pytest.raises(L.OombError) as e:
+        L.oomb_check(pool.handle)
+    assert e.value.status == 5
+    # a valid selection afterwards: no error
+    gsel, gcnt = pad_sel([np.array(good)] * w.n_kv_heads, max_sel, dev)
+    L.oomb_chunk_attn_fwd(pool.handle, q, start, gsel, gcnt, scale, o, lse)
+    L.oomb_chunk_attn_bwd(pool.handle, q, o, do, lse, start, gsel, gcnt, scale, dq, ws)
+    assert L.oomb_check(pool.handle) == 0
+    pool.close()
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
