@@ -152,14 +152,15 @@ class Step:
         # a long attention grid's pending blocks
         self.side = torch.cuda.Stream(device=dev, priority=-1) if self.offload else None
 
-    def run(self, record=False, no_recompute=False, wait_in=None, on_dq=None):
+    def run(self, record=False, no_recompute=False, wait_in=None, on_dq=None, on_fwd=None):
         """One step.  The reverse sweep recomputes each chunk's O and LSE (activations are
         not kept).  With no_recompute the forward sweep's outputs are kept per chunk and
         the reverse sweep only runs the backward (the variant without recomputation).
         wait_in[c]: an event the step waits for before it first reads chunk c's inputs;
-        on_dq(c): called once chunk c's dQ has been issued (end-to-end copies)."""
+        on_fwd(c): called once chunk c's append has been issued, on_dq(c): once chunk
+        c's dQ has been issued (end-to-end copies)."""
         if self.offload:
-            return self.run_offload(record, wait_in=wait_in, on_dq=on_dq)
+            return self.run_offload(record, wait_in=wait_in, on_dq=on_dq, on_fwd=on_fwd)
         L, w, h, torch = self.L, self.w, self.pool.handle, self.torch
         L.oomb_pool_reset(h)
         for c, ch in enumerate(self.chunks):
@@ -167,6 +168,8 @@ class Step:
             if wait_in is not None:
                 torch.cuda.current_stream(self.dev).wait_event(wait_in[c])
             self._timed(record, self.app_events, c, L.oomb_kv_append, h, ch["k"], ch["v"], start)
+            if on_fwd is not None:
+                on_fwd(c)
             self._select(c, ch, start, n, record)
             if no_recompute:
                 if c not in self.o_keep:
@@ -190,7 +193,7 @@ class Step:
             if on_dq is not None:
                 on_dq(c)
 
-    def run_offload(self, record=False, wait_in=None, on_dq=None):
+    def run_offload(self, record=False, wait_in=None, on_dq=None, on_fwd=None):
         """K/V pools (and, with offload_grads, the fp32 dK/dV pools) in pinned host memory.
         The side stream moves the selected blocks of the next chunk into the other
         staging buffer while the main stream runs the current chunk's attention (forward
@@ -206,12 +209,17 @@ class Step:
         L.oomb_pool_reset(h)
 
         def append_select(c):
+            """Selection (it needs the history only), then the append, which also writes
+            the chunk's own pages into their staging slots of buffer c % 2."""
             start, n = w.chunk_bounds(c)
             ch = self.chunks[c]
             if wait_in is not None:
                 main.wait_event(wait_in[c])
-            self._timed(record, self.app_events, c, L.oomb_kv_append, h, ch["k"], ch["v"], start)
             self._select(c, ch, start, n, record)
+            self._timed(record, self.app_events, c, L.oomb_kv_append_staged, h, ch["k"], ch["v"], start,
+                        self.cnt[c], w.max_sel, c % 2)
+            if on_fwd is not None:
+                on_fwd(c)
 
         def side_timed(c, fn):
             if record:
@@ -223,13 +231,19 @@ class Step:
                 self.prefetch_events.append((p0, p1, c))
 
         def prefetch(c, after, prev=None):
-            """K/V of chunk c (and in the reverse sweep its gradient blocks not shared
-            with chunk prev) into staging buffer c % 2; returns the side-stream event."""
+            """K/V of chunk c into staging buffer c % 2 -- in the forward sweep (prev False)
+            the history pages only, the append having staged the own pages -- and in the
+            reverse sweep its gradient blocks not shared with chunk prev; returns the
+            side-stream event."""
             for e in after:
                 side.wait_event(e)
 
             def work():
-                L.oomb_prefetch(h, self.sel[c], self.cnt[c], c % 2, stream=side)
+                if prev is False:
+                    L.oomb_prefetch_pages(h, self.sel[c], self.cnt[c], c % 2, 0, w.chunk_bounds(c)[0] // w.page,
+                                          stream=side)
+                else:
+                    L.oomb_prefetch(h, self.sel[c], self.cnt[c], c % 2, stream=side)
                 if prev is not False and grads:
                     psel = self.sel[prev] if prev is not None else None
                     pcnt = self.cnt[prev] if prev is not None else None
@@ -316,9 +330,11 @@ class Step:
         for c in range(w.n_chunks):
             start, n = w.chunk_bounds(c)
             n_pages = -(-n // w.page)
-            # read K,V; write K,V; zero dK,dV rows (whole pages); summary rows
-            app[c] = (n * w.n_kv_heads * w.head_dim * esz * 2 * 2
-                      + n_pages * w.page * w.n_kv_heads * w.head_dim * 4 * 2
+            # read K,V; write K,V; zero dK,dV rows (whole pages; with the gradient pools in
+            # host memory a state byte per block instead); summary rows
+            zero = (n_pages * w.n_kv_heads if self.offload_grads
+                    else n_pages * w.page * w.n_kv_heads * w.head_dim * 4 * 2)
+            app[c] = (n * w.n_kv_heads * w.head_dim * esz * 2 * 2 + zero
                       + n_pages * w.n_kv_heads * w.head_dim * 4)
             n_hist = start // w.page
             cand = max(0, n_hist - w.n_sink)
@@ -384,6 +400,197 @@ class Step:
                 tot += int((mo * (start + n - ko) - mo * (mo - 1) // 2).sum())
             out.append(tot * w.group)
         return out
+
+
+class StackStep:
+    """A stack of attention layers over one sequence, K/V and gradient pools in pinned host
+    memory, run the way a model's forward and backward take them: chunk by chunk, the
+    layers in order (reversed in the reverse sweep).  The transfers follow the
+    explainer's 2.C: a local-window layer's history pages are staged one layer ahead
+    (its page set does not depend on its queries); a top-K layer's history pages move
+    while the layer's K/V projection runs (a synthetic GEMM of the layer's chunk, model
+    width 3584, that the selection does not wait for); the append writes the chunk's
+    own pages into their staging slots; in the reverse sweep every layer's K/V and
+    gradient blocks are staged one layer ahead.
+    One high-priority side stream carries every transfer."""
+
+    def __init__(self, w, n_layers, dev, model_dim=3584):
+        import torch
+
+        import paged_sparse_attention_gb300 as L
+        from paged_sparse_attention_gb300 import synth
+        self.L, self.torch, self.w, self.dev = L, torch, w, dev
+        self.side = torch.cuda.Stream(device=dev, priority=-1)
+        self.layers = []
+        for layer in range(n_layers):
+            st = Step(synth.stack_layer(w, layer), dev)
+            st.side = self.side
+            self.layers.append(st)
+        g = torch.Generator(device=dev)
+        g.manual_seed(w.base_seed)
+        self.X = torch.randn(w.chunk, model_dim, generator=g, device=dev).to(torch.bfloat16)
+        self.Wkv = (torch.randn(model_dim, 2 * w.n_kv_heads * w.head_dim, generator=g, device=dev)
+                    / math.sqrt(model_dim)).to(torch.bfloat16)
+        self.kv_acc = torch.empty(w.chunk, 2 * w.n_kv_heads * w.head_dim, dtype=torch.float32, device=dev)
+        self.gemm_ws = torch.empty(32 << 20, dtype=torch.uint8, device=dev)
+        self.gemm_flops = 2 * w.chunk * model_dim * 2 * w.n_kv_heads * w.head_dim
+        self.events = []  # (start, end) of every main-stream call, for the kernel time
+
+    def _main(self, record, fn, *args, **kw):
+        if not record:
+            return fn(*args, **kw)
+        e0, e1 = self.torch.cuda.Event(enable_timing=True), self.torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn(*args, **kw)
+        e1.record()
+        self.events.append((e0, e1))
+
+    def run(self, record=False):
+        L, w, torch = self.L, self.w, self.torch
+        main, side = torch.cuda.current_stream(self.dev), self.side
+        S, NL = w.n_chunks, len(self.layers)
+        ev = lambda: torch.cuda.Event()  # noqa: E731
+
+        def mark():
+            e = ev()
+            e.record(main)
+            return e
+
+        for st in self.layers:
+            L.oomb_pool_reset(st.pool.handle)
+        items = [(c, layer) for c in range(S) for layer in range(NL)]
+        staged = {}
+
+        def select_and_stage(c, layer):
+            """Selection of (c, layer) on the main stream, then its history pages staged."""
+            st = self.layers[layer]
+            start, n = w.chunk_bounds(c)
+            self._main(record, st._select, c, st.chunks[c], start, n, False)
+            e = mark()
+            side.wait_event(e)
+            L.oomb_prefetch_pages(st.pool.handle, st.sel[c], st.cnt[c], c % 2, 0, start // w.page, stream=side)
+            staged[(c, layer)] = True
+
+        for i, (c, layer) in enumerate(items):
+            st = self.layers[layer]
+            h = st.pool.handle
+            start, n = w.chunk_bounds(c)
+            if (c, layer) not in staged:
+                select_and_stage(c, layer)
+            if i + 1 < len(items):  # a local layer next: its page set is known, stage it now
+                c2, l2 = items[i + 1]
+                if self.layers[l2].w.window >= 0 and (c2, l2) not in staged:
+                    select_and_stage(c2, l2)
+            # the layer's K/V projection (synthetic) overlaps the history transfer; the
+            # append writes the chunk's own pages into their staging slots as well
+            self._main(record, L.oomb_gemm, self.X[:n], self.Wkv, self.kv_acc[:n], workspace=self.gemm_ws)
+            self._main(record, L.oomb_kv_append_staged, h, st.chunks[c]["k"], st.chunks[c]["v"], start, st.cnt[c],
+                       st.w.max_sel, c % 2)
+            done = ev()
+            done.record(side)  # every history transfer issued so far, this item's included
+            main.wait_event(done)
+            L.oomb_pool_set_stage(h, c % 2)
+            self._main(record, L.oomb_chunk_attn_fwd, h, st.chunks[c]["q"], start, st.sel[c], st.cnt[c], st.scale,
+                       st.ob[0][:n], st.lseb[0] if n == w.chunk else st.lse_tail(n))
+        # reverse sweep: every item's K/V and gradient blocks staged one item ahead
+        ritems = items[::-1]
+        bwd_done, ready = {}, {}
+
+        def stage_rev(c, layer):
+            st = self.layers[layer]
+            h = st.pool.handle
+            prev = c + 1 if c + 1 < S else None
+            if prev is not None:  # the carried blocks and the host blocks written back after it
+                side.wait_event(bwd_done[(prev, layer)])
+            L.oomb_prefetch(h, st.sel[c], st.cnt[c], c % 2, stream=side)
+            L.oomb_grad_prefetch(h, st.sel[c], st.cnt[c], st.sel[prev] if prev is not None else None,
+                                 st.cnt[prev] if prev is not None else None, c % 2, stream=side)
+            if prev is not None:
+                L.oomb_grad_carry(h, st.sel[c], st.cnt[c], st.sel[prev], st.cnt[prev], c % 2, stream=side)
+            r = ev()
+            r.record(side)
+            ready[(c, layer)] = r
+
+        side.wait_stream(main)  # the forward sweep's last reads of the staging buffers
+        stage_rev(*ritems[0])
+        for i, (c, layer) in enumerate(ritems):
+            st = self.layers[layer]
+            h = st.pool.handle
+            start, n = w.chunk_bounds(c)
+            if i + 1 < len(ritems):
+                c2, l2 = ritems[i + 1]
+                if c2 + 1 < S and (c2 + 1, l2) not in bwd_done:
+                    raise RuntimeError("stack order: the previous chunk of a layer must have run its backward")
+                stage_rev(c2, l2)
+            main.wait_event(ready[(c, layer)])
+            L.oomb_pool_set_stage(h, c % 2)
+            lse = st.lseb[0] if n == w.chunk else st.lse_tail(n)
+            self._main(record, L.oomb_chunk_attn_fwd, h, st.chunks[c]["q"], start, st.sel[c], st.cnt[c], st.scale,
+                       st.ob[0][:n], lse)
+            self._main(record, L.oomb_chunk_attn_bwd, h, st.chunks[c]["q"], st.ob[0][:n], st.chunks[c]["do"], lse,
+                       start, st.sel[c], st.cnt[c], st.scale, st.dq[c], st.ws_bwd)
+            bwd_done[(c, layer)] = mark()
+            side.wait_event(bwd_done[(c, layer)])
+            L.oomb_grad_writeback(h, st.sel[c], st.cnt[c], c % 2, stream=side)
+        main.wait_stream(side)
+
+    def pairs(self):
+        return [sum(st.pairs_per_chunk()) for st in self.layers]
+
+
+def run_stack(args, w, world, dev):
+    """--workload stack...: the multi-layer offload step; one JSON line."""
+    import torch
+
+    import paged_sparse_attention_gb300 as L
+    from paged_sparse_attention_gb300 import synth
+    n_layers = synth.STACK_LAYERS[w.name]
+    log(f"stack of {n_layers} layers ({w.name}): building inputs and pools")
+    stack = StackStep(w, n_layers, dev)
+    for i in range(max(3, args.warmup)):
+        stack.run()
+        torch.cuda.synchronize()
+        log(f"warm-up step {i} done")
+    for st in stack.layers:
+        L.oomb_check(st.pool.handle)
+    pairs = stack.pairs()
+    credited = sum(pairs) * 14 * w.head_dim
+    stack.events = []
+    launches0 = L.oomb_launch_count()
+    with ClockSampler(0 if not torch.cuda.is_available() else torch.cuda.current_device()) as clk:
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            stack.run(record=True)
+        e1.record()
+        torch.cuda.synchronize()
+    launches = L.oomb_launch_count() - launches0
+    ms = reduce_max_ms(e0.elapsed_time(e1) / args.steps, world, dev)
+    for st in stack.layers:
+        L.oomb_check(st.pool.handle)
+    kern_ms = sum(a.elapsed_time(b) for a, b in stack.events) / args.steps
+    exposed = max(0.0, ms - kern_ms)
+    gemm_ms_total = None
+    line = {"metric": METRIC, "value": round(job_throughput(credited, ms, world) / 1e12, 3), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": round(ms, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) Q/K/V/dO per layer, RoPE theta 1e6; no trained weights)",
+            "config": dict(config_of(w, world), layers=n_layers,
+                           layer_kinds=["top-%d" % w.top_k if i % 2 == 0 else "window-%d" % w.window
+                                        for i in range(n_layers)],
+                           kv_projection="synthetic GEMM per layer and chunk: [%d x 3584] x [3584 x %d] bf16"
+                                         % (w.chunk, 2 * w.n_kv_heads * w.head_dim)),
+            "tokens_per_s_per_layer": round(job_throughput(w.seq * n_layers, ms, world), 1),
+            "credited_tflop_per_step": credited / 1e12,
+            "main_stream_ms_per_step": round(kern_ms, 3),
+            "exposed_ms_per_step": round(exposed, 3),
+            "exposed_ms_per_layer": round(exposed / n_layers, 3),
+            "exposed_frac_of_step": round(exposed / ms, 4),
+            "gpu_launches": int(launches),
+            "clocks": clk.summary()}
+    del gemm_ms_total
+    print(json.dumps(line), flush=True)
 
 
 def state_bytes_per_10k(w) -> dict:
@@ -620,6 +827,11 @@ def main():
         if world > 1:
             dist.barrier()
 
+    if w.name in synth.STACK_LAYERS:
+        run_stack(args, w, world, dev)
+        if world > 1:
+            dist.destroy_process_group()
+        return
     log(f"workload {w.name}: building inputs and pool")
     step = Step(w, dev)
     torch.cuda.synchronize()
@@ -684,6 +896,8 @@ def main():
     app_ref = same_size_gbs(max(app_b.values()), dev, "copy") if app_gbs else None
     sel_ref = same_size_gbs(max(sel_b.values()), dev, "read") if sel_gbs else None
     hbm_peak = peaks.get("hbm_gbs", 6783.0)
+    # with offload the append writes K/V into host memory: its bound is the host link
+    app_peak = None
     value = job_throughput(credited, ms, world) / 1e12
     tokens_per_s = job_throughput(w.seq, ms, world)
     rec_ms = sum(a.elapsed_time(b) for a, b, _ in step.recompute_events) / args.steps
@@ -788,7 +1002,12 @@ def main():
                          "traffic": recorded_traffic(w.name, "oomb_chunk_attn_bwd"),
                          "traffic_unit": "DRAM bytes per launch (ncu dram__bytes_read.sum + write.sum)"},
             "append_call": {"gbs": round(app_gbs, 1) if app_gbs else None,
-                            "frac_of_hbm": round(app_gbs / hbm_peak, 3) if app_gbs else None,
+                            "frac_of_hbm": round(app_gbs / hbm_peak, 3) if app_gbs and not step.offload else None,
+                            "bound": "host link (K/V pools in pinned host memory)" if step.offload else "hbm",
+                            "host_write_gbs": (round(sum(w.chunk_bounds(c)[1] * w.n_kv_heads * w.head_dim * 2
+                                                         * (2 if w.dtype == "bf16" else 4) for _, _, c in step.app_events)
+                                                     / (sum(a.elapsed_time(b) for a, b, _ in step.app_events) * 1e-3)
+                                                     / 1e9, 1) if step.offload and step.app_events else None),
                             "same_size_copy_gbs": round(app_ref, 1) if app_ref else None,
                             "frac_of_same_size_copy": round(app_gbs / app_ref, 3) if app_ref else None,
                             "bytes_per_token_per_kv_head": 2 * 2 * w.head_dim * (2 if w.dtype == "bf16" else 4)
@@ -846,6 +1065,9 @@ class HostBuffer:
             self.buf = None
 
 
+E2E_AHEAD = 3  # chunks whose inputs are uploaded ahead of the forward sweep
+
+
 def measure_e2e(step, steps, credited, world, dev):
     """Same step with host-resident inputs: every step copies Q, K, V, dO of all
     chunks from page-locked host memory to the device and reads dQ (and, when the
@@ -878,16 +1100,31 @@ def measure_e2e(step, steps, credited, world, dev):
         bo += int(cnt_h.sum()) * 2 * w.page * w.head_dim * 4
     main = torch.cuda.current_stream(dev)
     copy = torch.cuda.Stream(device=dev)
+    S = len(step.chunks)
 
     def one_step():
         copy.wait_stream(main)  # the previous step has finished reading the input buffers
         ready = {}
-        with torch.cuda.stream(copy):
-            for c, (ch, hc) in enumerate(zip(step.chunks, host_in)):
-                for k in ch:
-                    ch[k].copy_(hc[k], non_blocking=True)
+
+        def upload(c):
+            with torch.cuda.stream(copy):
+                for k in step.chunks[c]:
+                    step.chunks[c][k].copy_(host_in[c][k], non_blocking=True)
                 ready[c] = torch.cuda.Event()
                 ready[c].record(copy)
+
+        # paced: chunk c + AHEAD is uploaded once chunk c's append has been issued, so
+        # that the uploads spread over the forward sweep instead of taking the host
+        # link in one burst (the offload gathers share it)
+        for c in range(min(E2E_AHEAD, S)):
+            upload(c)
+
+        def on_fwd(c):
+            if c + E2E_AHEAD < S:
+                e = torch.cuda.Event()
+                e.record(main)
+                copy.wait_event(e)
+                upload(c + E2E_AHEAD)
 
         def on_dq(c):
             done = torch.cuda.Event()
@@ -896,7 +1133,7 @@ def measure_e2e(step, steps, credited, world, dev):
             with torch.cuda.stream(copy):
                 host_dq[c].copy_(step.dq[c], non_blocking=True)
 
-        step.run(wait_in=ready, on_dq=on_dq)
+        step.run(wait_in=ready, on_dq=on_dq, on_fwd=on_fwd)
         if pools_on_device:
             copy.wait_stream(main)
             with torch.cuda.stream(copy):
@@ -906,19 +1143,22 @@ def measure_e2e(step, steps, credited, world, dev):
 
     one_step()  # warm-up of the copy path
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(steps):
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    ev[0].record()
+    for i in range(steps):
         one_step()
-    e1.record()
+        ev[i + 1].record()
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / steps
+    per_step = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+    ms = ev[0].elapsed_time(ev[steps]) / steps
     hb.close()
     if pools_on_device:
         hp.close()
     return {"value": round(credited / (ms * 1e-3) / 1e12 * world, 3), "unit": UNIT, "ms_per_step": round(ms, 3),
+            "ms_per_step_min_max": [round(min(per_step), 3), round(max(per_step), 3)],
             "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
-            "overlap": "uploads per chunk on a copy stream; dQ read back as each backward is issued"}
+            "overlap": f"uploads per chunk on a copy stream, {E2E_AHEAD} chunks ahead of the forward sweep; "
+                       "dQ read back as each backward is issued"}
 
 
 if __name__ == "__main__":

@@ -140,6 +140,20 @@ OOMB_API void oomb_pool_destroy(oomb_pool* pool);
  * page-table entry to -1 (stream-ordered).  The pools' contents are kept. */
 OOMB_API oomb_status oomb_pool_reset(oomb_pool* pool, void* stream);
 
+/* Offload mode: oomb_kv_append, and the new pages also written into staging buffer
+ * stage_buf at the slots of the chunk's own pages, so that the chunk's attention
+ * needs only its history pages from host memory (oomb_prefetch_pages up to the
+ * chunk's first page).  The chunk's selection (top-K or window, computed before the
+ * append: a selection needs only the history) lists the own pages last: own page j
+ * of n_own goes to slot sel_count[h] - n_own + j of KV head h.  The append must
+ * cover exactly the chunk's tokens.  max_sel: the selection's row length (<=
+ * stage_max_sel).  A count smaller than n_own or above max_sel sets OOMB_DEVERR_SEL
+ * and that head's pages are not staged.
+ * Errors: those of oomb_kv_append, UNSUPPORTED (pool not in offload mode). */
+OOMB_API oomb_status oomb_kv_append_staged(oomb_pool* pool, const void* k, const void* v, int64_t first_token,
+                                           int n_tokens, const int32_t* sel_count, int max_sel, int stage_buf,
+                                           void* stream);
+
 /* Return logical pages [first_logical_page, first_logical_page + n_pages) to the
  * free list (explainer 2.B: fixed-size pages; "3. Key Contributions": paged
  * memory without fragmentation).  Every page of the range must be mapped (already
@@ -177,7 +191,9 @@ OOMB_API oomb_status oomb_kv_append(oomb_pool* pool, const void* k, const void* 
  * [q_start/P, ceil((q_start+n_q)/P)).  top_k < 0 keeps every page.
  * Output per KV head: ascending logical pages in sel[h*max_sel ...], count in
  * sel_count[h].  q: [n_q, Hq, d] device.  q_start must be a multiple of P and
- * the chunk's own K/V already appended.  Workspace: oomb_workspace_size(
+ * every page before the chunk appended; the chunk's own K/V may come later (the
+ * selection reads history pages only), so it can run before the chunk's K/V
+ * projection.  Workspace: oomb_workspace_size(
  * OOMB_OP_SELECT, n_q) bytes of device memory, contents scratch.
  * Launch: one cooperative kernel (one CTA per SM) whose phases meet at grid
  * barriers kept in the pool's control block, so selections on one pool must be
@@ -203,7 +219,9 @@ OOMB_API oomb_status oomb_page_select(oomb_pool* pool, const void* q, int64_t q_
  *    4 KV heads x head_dim 128).
  *  - Set-up: the first call on a device looks up the array's device address with
  *    cudaGetSymbolAddress while that device is current; make that first call
- *    before any stream capture.
+ *    before any stream capture.  The address is kept for the life of the process:
+ *    after cudaDeviceReset (which destroys the context and the array with it) do
+ *    not call this entry point again in that process.
  *  - Sharing: every call on a device uses the same array and leaves its contents
  *    behind; nothing in it needs to start at zero.  Calls that overlap on the GPU
  *    (different streams, or different host threads) race on the array: order
@@ -228,7 +246,8 @@ OOMB_API oomb_status oomb_page_select_noalloc(oomb_pool* pool, const void* q, in
  * int32; entries past the count are left as they were).  Feed the result to
  * oomb_chunk_attn_fwd/bwd (and oomb_prefetch) like a top-K selection.  Reads no
  * K/V and no workspace; one small kernel on the stream.  q_start must be a
- * multiple of P and the chunk's own K/V already appended.
+ * multiple of P and every page before the chunk appended (the chunk's own K/V may
+ * come later: the set is known before the chunk's K/V are).
  * Errors: ARG (window < 0, n_sink < 0, max_sel smaller than the set), ALIGN,
  * CUDA. */
 OOMB_API oomb_status oomb_window_select(oomb_pool* pool, int64_t q_start, int n_q, int window, int n_sink,
@@ -315,9 +334,55 @@ OOMB_API oomb_status oomb_grad_carry(oomb_pool* pool, const int32_t* sel, const 
 OOMB_API oomb_status oomb_grad_writeback(oomb_pool* pool, const int32_t* sel, const int32_t* sel_count, int max_sel,
                                          int stage_buf, void* stream);
 
+/* oomb_prefetch restricted to the selected pages in [first_page, end_page): e.g.
+ * the history pages of a chunk while its K/V projection runs (explainer 2.C: the
+ * sparse transfers overlap the K/V projection; for local layers, one layer ahead),
+ * then its own pages once they are appended.  Errors: those of oomb_prefetch. */
+OOMB_API oomb_status oomb_prefetch_pages(oomb_pool* pool, const int32_t* sel, const int32_t* sel_count, int max_sel,
+                                         int stage_buf, int64_t first_page, int64_t end_page, void* stream);
+
 /* Offload mode: staging buffer that following attention calls read (K/V, and
  * with offload_grads the dK/dV blocks the backward adds into). */
 OOMB_API oomb_status oomb_pool_set_stage(oomb_pool* pool, int stage_buf);
+
+/* ---------------------------------------------------------------- layer step
+ * The chunk-recurrent layer step around the attention path (explainer 2.A: the
+ * chunk's activations are recomputed in the reverse sweep; its K/V gradients, final
+ * once every later chunk has run its backward, flow back through the rotary
+ * embedding and the projections Q = X Wq + bq, K = X Wk + bk, V = X Wv + bv). */
+
+/* C[m, n] = alpha op(A) op(B) + beta C, row-major: op(A) is A stored [m, k]
+ * (trans_a = 0) or the transpose of A stored [k, m]; op(B) is B stored [k, n] or the
+ * transpose of B stored [n, k]; C is [m, n].  A and B are dtype_ab (OOMB_BF16 or
+ * OOMB_FP32, both alike), C is dtype_c; fp32 accumulation, and fp32 operands are
+ * multiplied in full fp32 (no TF32).  A plain library GEMM (cuBLASLt) on `stream`,
+ * with the caller's device workspace (ws_bytes may be 0; 32 MiB lets every
+ * algorithm run); the first call on a device creates a cuBLASLt handle (a host
+ * object kept until exit).  Pointers 16-byte aligned.
+ * Errors: ARG, DTYPE, ALIGN, UNSUPPORTED (no algorithm for the shape), CUDA. */
+OOMB_API oomb_status oomb_gemm(int m, int n, int k, int trans_a, int trans_b, const void* a, const void* b, void* c,
+                               int dtype_ab, int dtype_c, float alpha, float beta, void* workspace, size_t ws_bytes,
+                               void* stream);
+
+/* out[i, h, :] = R(pos0 + i) (in[i, h, :] + bias[h, :]) for token rows i < n and heads
+ * h < H of a token-major [n, H, d] tensor (in may be a [n, H*d] GEMM output: the same
+ * memory).  R(t) is the rotate-half rotary embedding: each pair (j, j + d/2) turned by
+ * the angle t * theta^(-2j/d) (mode 1), by minus that angle (mode 2: the transpose,
+ * which carries gradients back), or not at all (mode 0: bias and cast only).  bias:
+ * fp32 [H*d] or NULL; in_dtype/out_dtype OOMB_BF16 or OOMB_FP32; in == out is allowed
+ * for equal dtypes.  The angles' cos/sin are computed in double precision.
+ * Errors: ARG (odd d, d > 128, theta <= 1 with a rotation), DTYPE, CUDA. */
+OOMB_API oomb_status oomb_bias_rope(const void* in, int in_dtype, const float* bias, void* out, int out_dtype, int n,
+                                    int H, int d, int64_t pos0, float theta, int mode, void* stream);
+
+/* dK, dV of tokens [first_token, first_token + n_tokens) read from the paged fp32
+ * gradient pool through the page table into token-major [n_tokens, Hkv, d] fp32
+ * (device).  With offload_grads the pools are in host memory and are read there: the
+ * blocks must have been written back (order the call after oomb_grad_writeback).
+ * An unmapped page sets OOMB_DEVERR_PAGE and its rows read as zero.
+ * Errors: ARG (range beyond the appended tokens), ALIGN, CUDA. */
+OOMB_API oomb_status oomb_grad_gather(oomb_pool* pool, int64_t first_token, int n_tokens, float* dk, float* dv,
+                                      void* stream);
 
 /* Bytes of device workspace `op` needs for a chunk of n_q queries (0 on error). */
 OOMB_API size_t oomb_workspace_size(const oomb_pool* pool, int op, int n_q);

@@ -13,7 +13,7 @@ recomputed on the fly just before the backward needs them; 2.B — K/V and their
 gradients live in pages and are accumulated in place; 2.D — top-K page retrieval
 (or, for the sparse layers of sparse-native models, a local window).
 
-Readings where the pages are silent (also in the design notes):
+Readings where the pages are silent:
 * the layer's trainable part on this path is the three projections
   Q = X Wq + bq, K = X Wk + bk, V = X Wv + bv (the biases are optional; Qwen2.5's
   projections carry them);

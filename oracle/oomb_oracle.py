@@ -22,9 +22,9 @@ podcast summary and a Chinese digest):
 * attention itself is textbook causal softmax attention with grouped KV heads,
   restricted to the keys of the selected pages.
 
-Readings taken where the pages are silent (each also listed in the design
-notes): the query side of the page score is the plain mean of the chunk's
-queries over all tokens and all query heads of the KV group; the sink is logical
+Readings taken where the pages are silent: the query side of the page score is
+the plain mean of the chunk's queries over all tokens and all query heads of the
+KV group; the sink is logical
 page 0 (``n_sink`` leading pages) and does not count toward K; the chunk's own
 pages are "local"; ties go to the lower *logical* page index; the causal mask is
 ``key position <= query position`` on absolute positions; LSE is the natural log
@@ -106,8 +106,8 @@ class OraclePool:
 
     def summary(self, p: int, h: int) -> np.ndarray:
         """Representative vector of a page: the mean key over the tokens present
-        (explainer, 2.D: top-K retrieval "based on a representative vector
-        average"; the mean key per page is the fixed scoring rule)."""
+        (explainer, 2.D: pages are ranked for top-K retrieval by an averaged
+        representative vector; the mean key per page is the fixed scoring rule)."""
         return self.page_keys(p, h).mean(axis=0)
 
     def gather(self, pages: Sequence[int], h: int):

@@ -63,11 +63,16 @@ def load(path: str = LIB_PATH) -> C.CDLL:
         "oomb_pool_destroy": (None, [vp]),
         "oomb_pool_reset": (i32, [vp, vp]),
         "oomb_kv_append": (i32, [vp, vp, vp, i64, i32, vp]),
+        "oomb_kv_append_staged": (i32, [vp, vp, vp, i64, i32, vp, i32, i32, vp]),
         "oomb_page_select": (i32, [vp, vp, i64, i32, i32, i32, vp, vp, i32, vp, sz, vp]),
         "oomb_chunk_attn_fwd": (i32, [vp, vp, i64, i32, vp, vp, i32, f32, vp, vp, vp]),
         "oomb_chunk_attn_bwd": (i32, [vp, vp, vp, vp, vp, i64, i32, vp, vp, i32, f32, vp, vp, sz, vp]),
         "oomb_prefetch": (i32, [vp, vp, vp, i32, i32, vp]),
         "oomb_pool_set_stage": (i32, [vp, i32]),
+        "oomb_prefetch_pages": (i32, [vp, vp, vp, i32, i32, i64, i64, vp]),
+        "oomb_gemm": (i32, [i32, i32, i32, i32, i32, vp, vp, vp, i32, i32, f32, f32, vp, sz, vp]),
+        "oomb_bias_rope": (i32, [vp, i32, vp, vp, i32, i32, i32, i32, i64, f32, i32, vp]),
+        "oomb_grad_gather": (i32, [vp, i64, i32, vp, vp, vp]),
         "oomb_grad_prefetch": (i32, [vp, vp, vp, i32, vp, vp, i32, vp]),
         "oomb_grad_carry": (i32, [vp, vp, vp, i32, vp, vp, i32, vp]),
         "oomb_grad_writeback": (i32, [vp, vp, vp, i32, i32, vp]),
@@ -133,6 +138,13 @@ def oomb_kv_append(pool: int, k, v, first_token: int, n_tokens: Optional[int] = 
     _ok("oomb_kv_append", load().oomb_kv_append(pool, _ptr(k), _ptr(v), first_token, n, _stream(stream)))
 
 
+def oomb_kv_append_staged(pool: int, k, v, first_token: int, sel_count, max_sel: int, stage_buf: int,
+                          n_tokens: Optional[int] = None, stream=None) -> None:
+    n = k.shape[0] if n_tokens is None else n_tokens
+    _ok("oomb_kv_append_staged", load().oomb_kv_append_staged(pool, _ptr(k), _ptr(v), first_token, n, _ptr(sel_count),
+                                                              max_sel, stage_buf, _stream(stream)))
+
+
 def oomb_page_select(pool: int, q, q_start: int, top_k: int, n_sink: int, sel, sel_count, workspace,
                      n_q: Optional[int] = None, stream=None) -> None:
     n = q.shape[0] if n_q is None else n_q
@@ -174,6 +186,39 @@ def oomb_prefetch(pool: int, sel, sel_count, stage_buf: int, stream=None) -> Non
                                               _stream(stream)))
 
 
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return OOMB_FP32
+    if t.dtype == torch.bfloat16:
+        return OOMB_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def oomb_gemm(a, b, c, trans_a: bool = False, trans_b: bool = False, alpha: float = 1.0, beta: float = 0.0,
+              workspace=None, stream=None) -> None:
+    """c[m, n] = alpha op(a) op(b) + beta c (row-major, contiguous tensors)."""
+    m, n = c.shape
+    k = a.shape[0] if trans_a else a.shape[1]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _ok("oomb_gemm", load().oomb_gemm(m, n, k, int(trans_a), int(trans_b), _ptr(a), _ptr(b), _ptr(c), _dtype_code(a),
+                                      _dtype_code(c), alpha, beta, _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def oomb_bias_rope(x_in, bias, x_out, n_heads: int, pos0: int, theta: float, mode: int, stream=None) -> None:
+    """x_out[i, h, :] = rotation(pos0 + i) (x_in[i, h, :] + bias[h, :]); mode 0 none, 1 forward, 2 inverse."""
+    n = x_in.shape[0]
+    d = x_in.numel() // (n * n_heads)
+    _ok("oomb_bias_rope", load().oomb_bias_rope(_ptr(x_in), _dtype_code(x_in), _ptr(bias), _ptr(x_out),
+                                                _dtype_code(x_out), n, n_heads, d, pos0, theta, mode,
+                                                _stream(stream)))
+
+
+def oomb_grad_gather(pool: int, first_token: int, dk, dv, stream=None) -> None:
+    _ok("oomb_grad_gather", load().oomb_grad_gather(pool, first_token, dk.shape[0], _ptr(dk), _ptr(dv),
+                                                    _stream(stream)))
+
+
 def oomb_grad_prefetch(pool: int, sel, sel_count, prev_sel, prev_count, stage_buf: int, stream=None) -> None:
     _ok("oomb_grad_prefetch", load().oomb_grad_prefetch(pool, _ptr(sel), _ptr(sel_count), sel.shape[-1],
                                                         _ptr(prev_sel), _ptr(prev_count), stage_buf,
@@ -188,6 +233,12 @@ def oomb_grad_carry(pool: int, sel, sel_count, prev_sel, prev_count, stage_buf: 
 def oomb_grad_writeback(pool: int, sel, sel_count, stage_buf: int, stream=None) -> None:
     _ok("oomb_grad_writeback", load().oomb_grad_writeback(pool, _ptr(sel), _ptr(sel_count), sel.shape[-1],
                                                           stage_buf, _stream(stream)))
+
+
+def oomb_prefetch_pages(pool: int, sel, sel_count, stage_buf: int, first_page: int, end_page: int,
+                        stream=None) -> None:
+    _ok("oomb_prefetch_pages", load().oomb_prefetch_pages(pool, _ptr(sel), _ptr(sel_count), sel.shape[-1], stage_buf,
+                                                          first_page, end_page, _stream(stream)))
 
 
 def oomb_pool_set_stage(pool: int, stage_buf: int) -> None:

@@ -1,6 +1,7 @@
 // C-ABI layer: pool object, host-side page allocator, argument checks and
 // dispatch to the kernels.  No call here allocates device memory.
 #include <atomic>
+#include <climits>
 #include <cstring>
 #include <new>
 
@@ -107,13 +108,17 @@ KvSource kv_source(const oomb_pool* p) {
   return s;
 }
 
-// Checks shared by the chunk-level calls.
+// Checks shared by the chunk-level calls.  `own_appended`: the chunk's own K/V must
+// already be in the pool (attention); a selection reads history pages only, so it
+// needs just the history.
 oomb_status check_chunk(const oomb_pool* p, const void* q, int64_t q_start, int n_q, const int32_t* sel,
-                        const int32_t* sel_count, int max_sel) {
+                        const int32_t* sel_count, int max_sel, bool own_appended = true) {
   if (!p || !q || !sel || !sel_count) return OOMB_ERR_ARG;
   if (n_q <= 0 || q_start < 0 || max_sel <= 0) return OOMB_ERR_ARG;
   if (q_start % p->g.P != 0) return OOMB_ERR_ALIGN;
-  if (q_start + n_q > p->n_tokens) return OOMB_ERR_ARG;  // own K/V must be appended
+  if (q_start > p->n_tokens) return OOMB_ERR_ARG;                       // the history
+  if (own_appended && q_start + n_q > p->n_tokens) return OOMB_ERR_ARG;  // own K/V
+  if (q_start + n_q > (int64_t)p->g.max_logical * p->g.P) return OOMB_ERR_ARG;
   if (!aligned(q, 16) || !aligned(sel, 4) || !aligned(sel_count, 4)) return OOMB_ERR_ALIGN;
   return OOMB_OK;
 }
@@ -211,8 +216,9 @@ uint64_t oomb_launch_count(void) { return g_launches.load(std::memory_order_rela
 
 int oomb_uses_tensor_cores(const oomb_pool* p) { return p && tc_supported(p->g) ? 1 : 0; }
 
-oomb_status oomb_kv_append(oomb_pool* p, const void* k, const void* v, int64_t first_token, int n_tokens,
-                           void* stream) {
+// Shared body of oomb_kv_append and oomb_kv_append_staged.
+static oomb_status kv_append_impl(oomb_pool* p, const void* k, const void* v, int64_t first_token, int n_tokens,
+                                  const StageArgs* stage, void* stream) {
   if (!p || !k || !v || n_tokens <= 0 || first_token < 0) return OOMB_ERR_ARG;
   if (first_token != p->n_tokens) return OOMB_ERR_ARG;
   if (first_token % p->g.P != 0) return OOMB_ERR_ALIGN;
@@ -234,7 +240,7 @@ oomb_status oomb_kv_append(oomb_pool* p, const void* k, const void* v, int64_t f
   }
   e = launch_kv_append(p->g, p->d.k_pool, p->d.v_pool, p->d.dk_pool, p->d.dv_pool, p->d.summary,
                                    p->d.page_table, k, v, first_token, n_tokens, end, newp.data(), n_new,
-                                   (int)first_page, p->d.offload_grads ? p->d.grad_state : nullptr,
+                                   (int)first_page, p->d.offload_grads ? p->d.grad_state : nullptr, stage,
                                    p->d.error_word, (cudaStream_t)stream);
   if (e != cudaSuccess) {
     for (int i = n_new - 1; i >= 0; --i) {
@@ -245,6 +251,27 @@ oomb_status oomb_kv_append(oomb_pool* p, const void* k, const void* v, int64_t f
   }
   p->n_tokens = end;
   return OOMB_OK;
+}
+
+oomb_status oomb_kv_append(oomb_pool* p, const void* k, const void* v, int64_t first_token, int n_tokens,
+                           void* stream) {
+  return kv_append_impl(p, k, v, first_token, n_tokens, nullptr, stream);
+}
+
+oomb_status oomb_kv_append_staged(oomb_pool* p, const void* k, const void* v, int64_t first_token, int n_tokens,
+                                  const int32_t* sel_count, int max_sel, int stage_buf, void* stream) {
+  if (!p || !sel_count || max_sel <= 0) return OOMB_ERR_ARG;
+  if (!p->d.offload) return OOMB_ERR_UNSUPPORTED;
+  if (stage_buf < 0 || stage_buf > 1 || max_sel > p->d.stage_max_sel) return OOMB_ERR_ARG;
+  if (!aligned(sel_count, 4)) return OOMB_ERR_ALIGN;
+  StageArgs sa;
+  sa.k = p->d.stage_k;
+  sa.v = p->d.stage_v;
+  sa.sel_count = sel_count;
+  sa.stage_h0 = stage_buf * p->g.Hkv;
+  sa.stride = p->d.stage_max_sel;
+  sa.max_sel = max_sel;
+  return kv_append_impl(p, k, v, first_token, n_tokens, &sa, stream);
 }
 
 oomb_status oomb_page_free(oomb_pool* p, int64_t first_logical_page, int n_pages, void* stream) {
@@ -275,7 +302,7 @@ size_t oomb_workspace_size(const oomb_pool* p, int op, int n_q) {
 oomb_status oomb_page_select(oomb_pool* p, const void* q, int64_t q_start, int n_q, int top_k, int n_sink,
                              int32_t* sel, int32_t* sel_count, int max_sel, void* ws, size_t ws_bytes,
                              void* stream) {
-  oomb_status s = check_chunk(p, q, q_start, n_q, sel, sel_count, max_sel);
+  oomb_status s = check_chunk(p, q, q_start, n_q, sel, sel_count, max_sel, false);
   if (s != OOMB_OK) return s;
   if (top_k < -1 || n_sink < 0) return OOMB_ERR_ARG;
   const int P = p->g.P;
@@ -298,7 +325,7 @@ oomb_status oomb_window_select(oomb_pool* p, int64_t q_start, int n_q, int windo
   if (!p || !sel || !sel_count) return OOMB_ERR_ARG;
   if (n_q <= 0 || q_start < 0 || max_sel <= 0 || window < 0 || n_sink < 0) return OOMB_ERR_ARG;
   if (q_start % p->g.P != 0) return OOMB_ERR_ALIGN;
-  if (q_start + n_q > p->n_tokens) return OOMB_ERR_ARG;  // own K/V must be appended
+  if (q_start > p->n_tokens) return OOMB_ERR_ARG;  // the history must be appended
   if (!aligned(sel, 4) || !aligned(sel_count, 4)) return OOMB_ERR_ALIGN;
   const int P = p->g.P;
   const int64_t n_hist = q_start / P;
@@ -376,14 +403,20 @@ oomb_status oomb_chunk_attn_bwd(oomb_pool* p, const void* q, const void* o, cons
   return cuda_status(e);
 }
 
-oomb_status oomb_prefetch(oomb_pool* p, const int32_t* sel, const int32_t* sel_count, int max_sel, int stage_buf,
-                          void* stream) {
-  if (!p || !sel || !sel_count || max_sel <= 0) return OOMB_ERR_ARG;
+oomb_status oomb_prefetch_pages(oomb_pool* p, const int32_t* sel, const int32_t* sel_count, int max_sel,
+                                int stage_buf, int64_t first_page, int64_t end_page, void* stream) {
+  if (!p || !sel || !sel_count || max_sel <= 0 || first_page < 0 || end_page < first_page) return OOMB_ERR_ARG;
   if (!p->d.offload) return OOMB_ERR_UNSUPPORTED;
   if (stage_buf < 0 || stage_buf > 1 || max_sel > p->d.stage_max_sel) return OOMB_ERR_ARG;
+  const int lo = (int)std::min<int64_t>(first_page, INT32_MAX), hi = (int)std::min<int64_t>(end_page, INT32_MAX);
   return cuda_status(launch_prefetch(p->g, p->d.k_pool, p->d.v_pool, p->d.page_table, sel, sel_count, max_sel,
-                                     p->d.stage_k, p->d.stage_v, stage_buf * p->g.Hkv, p->d.stage_max_sel,
+                                     p->d.stage_k, p->d.stage_v, stage_buf * p->g.Hkv, p->d.stage_max_sel, lo, hi,
                                      p->d.error_word, (cudaStream_t)stream));
+}
+
+oomb_status oomb_prefetch(oomb_pool* p, const int32_t* sel, const int32_t* sel_count, int max_sel, int stage_buf,
+                          void* stream) {
+  return oomb_prefetch_pages(p, sel, sel_count, max_sel, stage_buf, 0, INT32_MAX, stream);
 }
 
 // Shared checks of the gradient staging calls.
@@ -423,6 +456,14 @@ oomb_status oomb_grad_writeback(oomb_pool* p, const int32_t* sel, const int32_t*
   return cuda_status(launch_grad_copy(p->g, kGradToHost, p->d.dk_pool, p->d.dv_pool, p->d.grad_state, p->d.page_table, sel,
                                       sel_count, nullptr, nullptr, max_sel, p->d.stage_dk, p->d.stage_dv, stage_buf,
                                       p->d.stage_max_sel, p->d.error_word, (cudaStream_t)stream));
+}
+
+oomb_status oomb_grad_gather(oomb_pool* p, int64_t first_token, int n_tokens, float* dk, float* dv, void* stream) {
+  if (!p || !dk || !dv || n_tokens <= 0 || first_token < 0) return OOMB_ERR_ARG;
+  if (first_token + n_tokens > p->n_tokens) return OOMB_ERR_ARG;
+  if (!aligned(dk, 16) || !aligned(dv, 16)) return OOMB_ERR_ALIGN;
+  return cuda_status(launch_grad_gather(p->g, p->d.dk_pool, p->d.dv_pool, p->d.page_table, first_token, n_tokens,
+                                        dk, dv, p->d.error_word, (cudaStream_t)stream));
 }
 
 oomb_status oomb_pool_set_stage(oomb_pool* p, int stage_buf) {

@@ -53,11 +53,21 @@ struct AttnArgs {
   size_t ws_bytes;
 };
 
+// Offload mode: the new pages of an append also go to the staging slots of the
+// chunk's own pages (the last entries of each KV head's selection).
+struct StageArgs {
+  void* k;
+  void* v;
+  const int32_t* sel_count;
+  int stage_h0, stride, max_sel;
+};
+
 // ---- launchers (return cudaGetLastError of the launch) ----
 cudaError_t launch_kv_append(const Geometry& g, void* k_pool, void* v_pool, float* dk_pool, float* dv_pool,
                              float* summary, int32_t* table, const void* k, const void* v, int64_t first_token,
                              int n_tokens, int64_t total_tokens, const int32_t* new_phys, int n_new,
-                             int first_new_logical, uint8_t* grad_state, uint32_t* err, cudaStream_t st);
+                             int first_new_logical, uint8_t* grad_state, const StageArgs* stage, uint32_t* err,
+                             cudaStream_t st);
 
 size_t select_workspace_bytes(const Geometry& g, int n_q);
 cudaError_t launch_page_select(const Geometry& g, const float* summary, const int32_t* table, const void* q,
@@ -78,7 +88,8 @@ size_t bwd_tc_workspace_bytes(const Geometry& g, int n_q);
 
 cudaError_t launch_prefetch(const Geometry& g, const void* k_pool, const void* v_pool, const int32_t* table,
                             const int32_t* sel, const int32_t* sel_count, int max_sel, void* stage_k, void* stage_v,
-                            int stage_h0, int stage_stride, uint32_t* err, cudaStream_t st);
+                            int stage_h0, int stage_stride, int first_page, int end_page, uint32_t* err,
+                            cudaStream_t st);
 
 // Gradient staging (offload mode with host-resident dK/dV pools).  mode 0: stage the
 // blocks of `sel` whose page is not in `prev` from the host pools; mode 1: copy the
@@ -89,6 +100,10 @@ cudaError_t launch_grad_copy(const Geometry& g, int mode, float* dk_pool, float*
                              const int32_t* table, const int32_t* sel, const int32_t* sel_count,
                              const int32_t* prev_sel, const int32_t* prev_count, int max_sel, float* stage_dk,
                              float* stage_dv, int buf, int stage_stride, uint32_t* err, cudaStream_t st);
+
+cudaError_t launch_grad_gather(const Geometry& g, const float* dk_pool, const float* dv_pool, const int32_t* table,
+                               int64_t first_token, int n_tokens, float* dk, float* dv, uint32_t* err,
+                               cudaStream_t st);
 
 __host__ __device__ inline size_t dtype_size(int dt) { return dt == OOMB_FP32 ? 4 : 2; }
 // Count of kernel launches issued by the library (reported by oomb_launch_count).

@@ -85,17 +85,21 @@ __device__ __forceinline__ int selected_phys(const Geometry& g, const int32_t* t
 }
 
 // item = (s, h, which) in s-major order: slot (stage_h0 + h) * stride + s  <-  pool block
-// (phi(sel[h][s]), h), for every item of the chunk's selection.
+// (phi(sel[h][s]), h), for every item of the chunk's selection whose logical page is in
+// [first_page, end_page).
 __global__ void __launch_bounds__(kCopyThreads, 8)
     gather_pages(Geometry g, const uint8_t* __restrict__ k_pool, const uint8_t* __restrict__ v_pool,
                  const int32_t* __restrict__ table, const int32_t* __restrict__ sel,
                  const int32_t* __restrict__ sel_count, int max_sel, uint8_t* __restrict__ stage_k,
-                 uint8_t* __restrict__ stage_v, int stage_h0, int stride, uint32_t* err) {
+                 uint8_t* __restrict__ stage_v, int stage_h0, int stride, int first_page, int end_page,
+                 uint32_t* err) {
   const size_t bytes = (size_t)g.P * g.d * dtype_size(g.dtype);
   const int n_items = max_sel * g.Hkv * 2;
   for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
     const int which = it & 1, h = (it >> 1) % g.Hkv, s = (it >> 1) / g.Hkv;
     if (s >= checked_count(sel_count, h, max_sel, err)) continue;
+    const int pg = sel[(size_t)h * max_sel + s];
+    if (pg >= 0 && (pg < first_page || pg >= end_page)) continue;  // outside the requested pages
     int p;
     const int phys = selected_phys(g, table, sel, max_sel, h, s, &p, err);
     if (phys < 0) continue;
@@ -162,11 +166,12 @@ __global__ void __launch_bounds__(kCopyThreads, 8)
 
 cudaError_t launch_prefetch(const Geometry& g, const void* k_pool, const void* v_pool, const int32_t* table,
                             const int32_t* sel, const int32_t* sel_count, int max_sel, void* stage_k, void* stage_v,
-                            int stage_h0, int stage_stride, uint32_t* err, cudaStream_t st) {
+                            int stage_h0, int stage_stride, int first_page, int end_page, uint32_t* err,
+                            cudaStream_t st) {
   const int grid = std::min(max_sel * g.Hkv * 2, kCopyCtas);
   gather_pages<<<grid, kCopyThreads, 0, st>>>(g, (const uint8_t*)k_pool, (const uint8_t*)v_pool, table, sel,
                                               sel_count, max_sel, (uint8_t*)stage_k, (uint8_t*)stage_v, stage_h0,
-                                              stage_stride, err);
+                                              stage_stride, first_page, end_page, err);
   count_launches(1);
   return cudaGetLastError();
 }

@@ -105,6 +105,11 @@ __device__ __forceinline__ float4 ld_dsmem_f4(uint32_t caddr) {
                : "memory");
   return v;
 }
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t caddr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(caddr) : "memory");
+  return v;
+}
 // Arrive on an mbarrier of another CTA of the cluster (release at cluster scope).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t caddr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");

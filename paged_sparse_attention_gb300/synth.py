@@ -100,7 +100,23 @@ WORKLOADS: Dict[str, Workload] = {
     # chunk's own pages, no sink and no top-K.
     "window128k": Workload("window128k", 28, 4, 128, "bf16", 131072, 4096, 128, -1, n_sink=0,
                            rope=True, base_seed=1005, window=32),
+    # A stack of 4 layers over 256K tokens in chunks of 8192, K/V and gradients in pinned
+    # host memory: even layers retrieve the top-128 pages, odd layers attend to a local
+    # window of 32 pages (the sparse layers of a sparse-native model); each layer draws
+    # its own seeded tensors (the base seed plus 101 per layer).
+    "stack4x256k": Workload("stack4x256k", 28, 4, 128, "bf16", 262144, 8192, 128, 128,
+                            rope=True, plants=8, base_seed=1006, offload=True, offload_grads=True, window=32),
 }
+
+STACK_LAYERS = {"stack4x256k": 4}
+
+
+def stack_layer(w: Workload, layer: int) -> Workload:
+    """Layer ``layer`` of a stack workload: top-K retrieval on even layers, the local
+    window on odd ones, and its own seed."""
+    local = layer % 2 == 1
+    return dataclasses.replace(w, name=f"{w.name}_layer{layer}", base_seed=w.base_seed + 101 * (layer + 1),
+                               window=w.window if local else -1, plants=0 if local else w.plants)
 
 
 def scaled(w: Workload, name: str, **kw) -> Workload:

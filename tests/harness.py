@@ -51,7 +51,8 @@ class GpuSweep:
     the staging buffer of its parity before its attention calls."""
 
     def __init__(self, w: synth.Workload, chunks, order, dev="cuda", sel_override=None, scale=None,
-                 num_phys: Optional[int] = None, offload: bool = False, offload_grads: bool = False):
+                 num_phys: Optional[int] = None, offload: bool = False, offload_grads: bool = False,
+                 staged_append: bool = False):
         self.w = w
         self.dev = torch.device(dev)
         self.scale = 1.0 / math.sqrt(w.head_dim) if scale is None else scale
@@ -83,17 +84,25 @@ class GpuSweep:
             start, n = w.chunk_bounds(c)
             g = {k: v.to(self.dev) for k, v in ch.items()}
             dev_chunks.append(g)
-            L.oomb_kv_append(h, g["k"], g["v"], start)
+            if not staged_append:
+                L.oomb_kv_append(h, g["k"], g["v"], start)
             sel = torch.full((w.n_kv_heads, max_sel), -1, dtype=torch.int32, device=self.dev)
             cnt = torch.zeros(w.n_kv_heads, dtype=torch.int32, device=self.dev)
-            if w.window >= 0:
+            if w.window >= 0:  # a selection needs the history only
                 L.oomb_window_select(h, start, n, w.window, w.n_sink, sel, cnt)
             else:
                 L.oomb_page_select(h, g["q"], start, w.top_k, w.n_sink, sel, cnt, ws_sel)
             self.gpu_sel.append([sel[i, : int(cnt[i])].cpu().numpy() for i in range(w.n_kv_heads)])
             if sel_override is not None:
                 sel, cnt = pad_sel(sel_override[c], max_sel, self.dev)
-            stage(c, sel, cnt)
+            if staged_append:  # own pages into their staging slots; only the history comes from the host
+                L.oomb_kv_append_staged(h, g["k"], g["v"], start, cnt, max_sel, c % 2)
+                side.wait_stream(main)
+                L.oomb_prefetch_pages(h, sel, cnt, c % 2, 0, start // w.page, stream=side)
+                main.wait_stream(side)
+                L.oomb_pool_set_stage(h, c % 2)
+            else:
+                stage(c, sel, cnt)
             o = torch.empty_like(g["q"])
             lse = torch.empty(w.n_q_heads, n, dtype=torch.float32, device=self.dev)
             L.oomb_chunk_attn_fwd(h, g["q"], start, sel, cnt, self.scale, o, lse)

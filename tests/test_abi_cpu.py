@@ -69,8 +69,11 @@ def test_allocator_host_logic(lib):
     assert lib.oomb_pool_free_pages(pool) == 4
     # chunk-level calls before the chunk's K/V exist
     assert lib.oomb_chunk_attn_fwd(pool, fake, 0, 128, fake, fake, 8, 0.1, fake, fake, None) == 1
-    assert lib.oomb_page_select(pool, fake, 0, 128, 4, 1, fake, fake, 8, fake, 1 << 30, None) == 1
-    assert lib.oomb_window_select(pool, 0, 128, 2, 1, fake, fake, 8, None) == 1  # chunk not appended
+    # a selection needs the history only (its chunk's own K/V may come later): a chunk
+    # that starts after the appended tokens is refused
+    assert lib.oomb_page_select(pool, fake, 128, 128, 4, 1, fake, fake, 8, fake, 1 << 30, None) == 1
+    assert lib.oomb_window_select(pool, 128, 128, 2, 1, fake, fake, 8, None) == 1  # history not appended
+    assert lib.oomb_page_select(pool, fake, 0, 256, 4, 1, fake, fake, 1, fake, 1 << 30, None) == 1  # max_sel < own
     assert lib.oomb_page_free(pool, 0, 1, None) == 1  # nothing appended yet
     assert lib.oomb_page_free(pool, -1, 1, None) == 1 and lib.oomb_page_free(pool, 0, 0, None) == 1
     assert lib.oomb_window_select(pool, 0, 128, -1, 1, fake, fake, 8, None) == 1  # negative window

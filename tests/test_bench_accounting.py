@@ -81,10 +81,13 @@ def test_algorithmic_bytes_per_call():
     written set; state per 10K tokens: K/V bf16 + dK/dV fp32 + summaries (K/V on
     the host with offload)."""
     w = synth.WORKLOADS["sparse128k"]
-    ns = types.SimpleNamespace(w=w)
+    ns = types.SimpleNamespace(w=w, offload_grads=False)
     app, sel = bench.Step.hbm_bytes(ns)
     C, Hkv, Hq, d, P = w.chunk, w.n_kv_heads, w.n_q_heads, w.head_dim, w.page
     assert app[5] == C * Hkv * 2048 + (C // P) * Hkv * d * 4
+    # gradient pools in host memory: no zeroing, one state byte per (page, KV head)
+    app_off, _ = bench.Step.hbm_bytes(types.SimpleNamespace(w=w, offload_grads=True))
+    assert app_off[5] == C * Hkv * 1024 + (C // P) * Hkv + (C // P) * Hkv * d * 4
     c = w.n_chunks - 1
     n_cand = c * C // P - w.n_sink
     assert sel[c] == C * Hq * d * 2 + n_cand * Hkv * d * 4 + 2 * n_cand * Hkv * 4 + Hkv * w.max_sel * 4

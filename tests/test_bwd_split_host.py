@@ -23,7 +23,7 @@ def test_split_policy_on_benchmark_shapes():
     os.makedirs(out_dir, exist_ok=True)
     exe = os.path.join(out_dir, "bwd_split_host")
     cmd = [nvcc, *build.ARCH, "-std=c++17", os.path.join(ROOT, "tests", "bwd_split_host.cpp"), *objs, "-o", exe,
-           "-lcuda", "-lcudart"]
+           "-lcuda", "-lcudart", "-lcublasLt"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0 and "cannot find -lcuda" in r.stderr:
         cmd.remove("-lcuda")

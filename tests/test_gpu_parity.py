@@ -196,21 +196,26 @@ def test_host_errors_on_gpu():
     pool.close()
 
 
-@pytest.mark.parametrize("grads", [False, True], ids=["kv", "kv+grads"])
+@pytest.mark.parametrize("grads,staged", [(False, False), (True, False), (True, True)],
+                         ids=["kv", "kv+grads", "kv+grads+staged-append"])
 @pytest.mark.parametrize("name", ["bf16_sparse", "fp32_sparse", "bf16_window"])
-def test_offload_matches_resident(name, grads):
+def test_offload_matches_resident(name, grads, staged):
     """K/V pools (and with grads the fp32 dK/dV pools) in pinned host memory, the
     selected blocks staged in HBM on a side stream (gradients staged in from the host
     or carried over from the previous chunk, and written back after each backward):
     the same outputs as the HBM-resident run -- bitwise for O, LSE, dK and dV (each
     gradient row is summed in a fixed order), dQ to rounding (fp32 reductions across
-    thread blocks in a run-dependent order) -- and within tolerance of the oracle."""
+    thread blocks in a run-dependent order) -- and within tolerance of the oracle.
+    With the staged append the selection comes first (it needs the history only), the
+    append writes the chunk's own pages into their staging slots, and only the history
+    pages are gathered from the host."""
     w = {**CASES, **WINDOW_CASES}[name]
     chunks, _ = make_chunks(w)
     order = synth.page_order(w).tolist()
     ref = oracle_sweep(w, chunks, order)
     res = GpuSweep(w, chunks, order, sel_override=ref["sel"])
-    off = GpuSweep(w, chunks, order, sel_override=ref["sel"], offload=True, offload_grads=grads)
+    off = GpuSweep(w, chunks, order, sel_override=ref["sel"], offload=True, offload_grads=grads,
+                   staged_append=staged)
     assert off.err_bits == 0
     for c in range(w.n_chunks):
         assert torch.equal(off.O[c], res.O[c]) and torch.equal(off.LSE[c], res.LSE[c])

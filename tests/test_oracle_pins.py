@@ -247,8 +247,8 @@ def test_planted_pages_selected():
 
 
 def test_planted_mistakes_are_caught(monkeypatch):
-    """A dropped term in the backward must fail the finite-difference pin, and a
-    flipped tie-break must fail the tie fixture."""
+    """A dropped term in the backward (D = rowsum(dO * O) left out) must fail the
+    dense-equivalence pin."""
     N, C, P, Hq, Hkv, d = 16, 8, 4, 2, 1, 4
     rng = np.random.default_rng(9)
     Q, K, V, dO = _rand_seq(rng, N, Hq, Hkv, d)
@@ -268,11 +268,61 @@ def test_planted_mistakes_are_caught(monkeypatch):
     assert O.rel_l2(np.concatenate(res_ok["dQ"]), dQd) < 1e-12
 
 
+def _select_ties_to_higher_page(pool, q, q_start, top_k, n_sink):
+    """A planted mistake: the oracle's selection with the tie-break reversed (ties go
+    to the higher logical page), everything else as in the oracle."""
+    n_hist = q_start // pool.P
+    own = np.arange(n_hist, (q_start + q.shape[0] - 1) // pool.P + 1)
+    sinks = np.arange(0, min(n_sink, n_hist))
+    cand, scores = O.page_scores(pool, q, q_start, n_sink)
+    out = []
+    for h in range(pool.Hkv):
+        order = np.lexsort((-cand, -scores[h]))
+        chosen = cand if cand.size <= top_k else cand[order[:top_k]]
+        out.append(np.sort(np.concatenate([sinks, chosen, own]).astype(np.int64)))
+    return out
+
+
+def test_planted_flipped_tie_break_fails_fixture():
+    """The hand-worked fixture has an exact tie at the K-th place: a selection that
+    gives ties to the higher page must disagree with it (and the oracle agrees)."""
+    with open(os.path.join(GOLDEN, "select_handworked.json")) as f:
+        g = json.load(f)
+    K = np.array(g["keys"], dtype=float)[:, None, :]
+    pool = O.OraclePool(1, K.shape[2], g["page_size"], g["num_phys"], g["num_phys"])
+    pool.append(K, K, 0, g["phys_order"][: len(K) // g["page_size"]])
+    q = np.array(g["queries"], dtype=float)[:, None, :]
+    n_own = -(-len(q) // g["page_size"])
+    pool.append(np.zeros((len(q), 1, K.shape[2])), np.zeros((len(q), 1, K.shape[2])), len(K),
+                g["phys_order"][len(K) // g["page_size"]: len(K) // g["page_size"] + n_own])
+    bad = _select_ties_to_higher_page(pool, q, len(K), g["top_k"], g["n_sink"])
+    assert bad[0].tolist() != g["expected_selection"]
+    assert O.select_pages(pool, q, len(K), g["top_k"], g["n_sink"])[0].tolist() == g["expected_selection"]
+
+
 def test_near_tie_rule():
     cand = np.arange(1, 6)
     scores = np.array([1.0, 0.5, 0.50000001, 0.2, 0.1])
+    # the swap of pages 2 and 3, tied to 1e-8 of max|score| at the K-th place: allowed
     assert O.near_tie_ok(np.array([0, 1, 2]), np.array([0, 1, 3]), cand, scores, 2)[0]
+    # page 4 (0.2) instead of page 3 (the K-th, 0.50000001): far from the boundary
     assert not O.near_tie_ok(np.array([0, 1, 4]), np.array([0, 1, 3]), cand, scores, 2)[0]
+
+
+def test_near_tie_rule_rejects_other_differences():
+    """Differences that no near-tie explains: a page more or fewer than the oracle
+    (even a near-tied one), a page outside the candidates, and a swap whose gap to the
+    K-th score is just above 1e-4 of max|score| (just below passes)."""
+    cand = np.arange(1, 7)
+    scores = np.array([1.0, 0.8, 0.6, 0.6 - 0.5e-4, 0.6 - 2e-4, 0.1])
+    ora = np.array([0, 1, 2, 3, 7])  # sink 0, top-3 {1, 2, 3}, own page 7
+    kth_swap = np.array([0, 1, 2, 4, 7])  # page 4 (gap 0.5e-4) for the K-th page 3
+    assert O.near_tie_ok(kth_swap, ora, cand, scores, 3)[0]
+    assert not O.near_tie_ok(np.array([0, 1, 2, 5, 7]), ora, cand, scores, 3)[0]  # gap 2e-4
+    assert not O.near_tie_ok(np.array([0, 1, 2, 3, 4, 7]), ora, cand, scores, 3)[0]  # one page more
+    assert not O.near_tie_ok(np.array([0, 1, 2, 7]), ora, cand, scores, 3)[0]  # one page fewer
+    assert not O.near_tie_ok(np.array([1, 2, 3, 4, 7]), ora, cand, scores, 3)[0]  # sink dropped for a near-tie
+    assert not O.near_tie_ok(np.array([0, 1, 2, 8, 7]), ora, cand, scores, 3)[0]  # not a candidate
 
 
 # -- local sliding-window selection ------------------------------------------------
