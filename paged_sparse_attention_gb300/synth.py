@@ -100,6 +100,11 @@ WORKLOADS: Dict[str, Workload] = {
     # chunk's own pages, no sink and no top-K.
     "window128k": Workload("window128k", 28, 4, 128, "bf16", 131072, 4096, 128, -1, n_sink=0,
                            rope=True, base_seed=1005, window=32),
+    # 128K tokens in chunks of 8192, top-128: the per-call shape of the 1M and 4M
+    # workloads (8192 queries, up to 1 + 128 + 64 selected pages) in ~2 GB of device
+    # memory, the case the kernel profiles are captured on.
+    "sparse128k_chunk8k": Workload("sparse128k_chunk8k", 28, 4, 128, "bf16", 131072, 8192, 128, 128,
+                                   rope=True, plants=8, base_seed=1007),
     # A stack of 4 layers over 256K tokens in chunks of 8192, K/V and gradients in pinned
     # host memory: even layers retrieve the top-128 pages, odd layers attend to a local
     # window of 32 pages (the sparse layers of a sparse-native model); each layer draws
