@@ -9,7 +9,7 @@
 // (zero-copy, 16-byte accesses), so a chunk's transfer is one launch on the side
 // stream instead of one copy call per block.
 //
-// Each launch is a small persistent grid (kCopyCtas thread blocks of 256 threads,
+// Each launch is a small persistent grid (8 or 16 thread blocks of 256 threads,
 // at most 32 registers each) that walks the chunk's blocks: a block fits on an SM
 // beside an attention CTA (one per SM, 320-448 threads), so the transfers run while
 // the attention kernels hold the SMs (issue them on a high-priority stream, or the
@@ -35,10 +35,14 @@ namespace {
 constexpr int kCopyThreads = 256;
 constexpr int kInFlight = 4;  // 16-byte loads per thread before the stores
 // Thread blocks of one transfer launch.  Measured on GB300 at 4M tokens (K/V and
-// gradients offloaded, side stream at high priority): 16 blocks move ~59 GB/s beside
-// the attention kernels with 74 ms of a 5.97 s step exposed; 32 and 64 move more but
-// slow the attention kernels on their SMs by more than they hide (step 5.99 / 6.27 s).
+// gradients offloaded, side stream at high priority): gradient copies with 16 blocks
+// move ~59 GB/s beside the attention kernels with 74 ms of a 5.97 s step exposed; 32
+// and 64 move more but slow the attention kernels on their SMs by more than they hide
+// (step 5.99 / 6.27 s).  K/V gathers need less (a forward-sweep chunk's history pages
+// in the ~2.3 ms of its forward): with 8 blocks instead of 16 the forward beside them
+// keeps ~1065 instead of ~1040 TFLOP/s at the same exposed time.
 constexpr int kCopyCtas = 16;
+constexpr int kGatherCtas = 8;
 
 // Copy `n16` 16-byte words from src to dst, kInFlight loads per thread in flight.
 __device__ __forceinline__ void copy_block(uint4* __restrict__ dst, const uint4* __restrict__ src, int n16) {
@@ -168,7 +172,7 @@ cudaError_t launch_prefetch(const Geometry& g, const void* k_pool, const void* v
                             const int32_t* sel, const int32_t* sel_count, int max_sel, void* stage_k, void* stage_v,
                             int stage_h0, int stage_stride, int first_page, int end_page, uint32_t* err,
                             cudaStream_t st) {
-  const int grid = std::min(max_sel * g.Hkv * 2, kCopyCtas);
+  const int grid = std::min(max_sel * g.Hkv * 2, kGatherCtas);
   gather_pages<<<grid, kCopyThreads, 0, st>>>(g, (const uint8_t*)k_pool, (const uint8_t*)v_pool, table, sel,
                                               sel_count, max_sel, (uint8_t*)stage_k, (uint8_t*)stage_v, stage_h0,
                                               stage_stride, first_page, end_page, err);
