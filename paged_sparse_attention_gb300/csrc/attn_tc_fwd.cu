@@ -318,13 +318,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       float mx[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) mx[k] = __uint_as_float(sr[k]);
+      for (int k = 0; k < 8; ++k) mx[k] = fmaxf(__uint_as_float(sr[k]), __uint_as_float(sr[8 + k]));
 #pragma unroll
-      for (int c = 8; c < 128; c += 8)
+      for (int c = 16; c < 128; c += 16)
 #pragma unroll
-        for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], __uint_as_float(sr[c + k]));
-      const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) *
+        for (int k = 0; k < 8; ++k)
+          mx[k] = fmax3(mx[k], __uint_as_float(sr[c + k]), __uint_as_float(sr[c + 8 + k]));
+      const float tmax = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) *
                          p.scale_log2;
       bool rescale_o = false;
       float alpha = 1.f;
@@ -336,11 +336,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         m = m_new;
       }
       const float neg_m = (m == -INFINITY) ? 0.f : -m;
+      // p = 2^(s * scale_log2 - m) two columns per packed FMA; two packed sum chains
+      const uint64_t scale2 = f32x2(p.scale_log2, p.scale_log2), negm2 = f32x2(neg_m, neg_m);
       float sum[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
-        const float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * c]), p.scale_log2, neg_m));
-        const float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * c + 1]), p.scale_log2, neg_m));
+        float t0, t1;
+        f32x2_split(ffma2(f32x2(sr[2 * c], sr[2 * c + 1]), scale2, negm2), t0, t1);
+        const float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
         sum[c & 3] += p0 + p1;
         sr[c] = pack_bf16x2(p0, p1);  // packed P: key columns 2c, 2c+1 -> column c
       }
