@@ -160,10 +160,10 @@ OOMB_API oomb_status oomb_kv_append_staged(oomb_pool* pool, const void* k, const
  * appended and not yet freed).  Their page-table entries become -1 on `stream`
  * and their physical pages are handed out first by the next appends (lowest
  * logical page first); the pool's token count is unchanged, so later appends
- * continue at the end.  A freed page must not be selected again: the attention
- * kernels and the top-K selection flag an unmapped page (OOMB_DEVERR_PAGE) and
- * skip it, so free only pages that no later selection reaches (pages behind a
- * local window, oomb_window_select; a finished sequence).
+ * continue at the end.  oomb_page_select leaves freed pages out (they are neither
+ * sinks nor candidates).  The attention kernels flag an unmapped page in a caller's
+ * selection (OOMB_DEVERR_PAGE) and skip it, and oomb_window_select does not look at
+ * the table, so with a local window free only the pages behind it.
  * Errors: ARG (range outside the appended pages, or a page not mapped), CUDA
  * (nothing changes on the host). */
 OOMB_API oomb_status oomb_page_free(oomb_pool* pool, int64_t first_logical_page, int n_pages, void* stream);
@@ -188,7 +188,9 @@ OOMB_API oomb_status oomb_kv_append(oomb_pool* pool, const void* k, const void* 
  * head h, every complete history page p in [n_sink, q_start/P) is scored as
  * qbar_h . summary[phi(p), h]; the top_k highest scores are kept (ties to the
  * lower logical page), plus pages [0, n_sink) and the chunk's own pages
- * [q_start/P, ceil((q_start+n_q)/P)).  top_k < 0 keeps every page.
+ * [q_start/P, ceil((q_start+n_q)/P)).  top_k < 0 keeps every page.  Pages freed
+ * by oomb_page_free are skipped: a freed sink is dropped and the top_k is taken
+ * over the mapped candidates (all of them when there are no more than top_k).
  * Output per KV head: ascending logical pages in sel[h*max_sel ...], count in
  * sel_count[h].  q: [n_q, Hq, d] device.  q_start must be a multiple of P and
  * every page before the chunk appended; the chunk's own K/V may come later (the
@@ -200,7 +202,8 @@ OOMB_API oomb_status oomb_kv_append(oomb_pool* pool, const void* k, const void* 
  * ordered (one stream, or events).  No host state changes between calls, so the
  * call may be captured in a CUDA graph.  A barrier wait that runs out (~1 s) sets
  * OOMB_DEVERR_TIMEOUT; oomb_check reports it and clears the control block.
- * Errors: ARG (incl. max_sel too small), ALIGN, WORKSPACE, CUDA. */
+ * Errors: ARG (incl. max_sel below the mapped sinks + kept candidates + own
+ * pages), ALIGN, WORKSPACE, CUDA. */
 OOMB_API oomb_status oomb_page_select(oomb_pool* pool, const void* q, int64_t q_start, int n_q, int top_k, int n_sink,
                              int32_t* sel, int32_t* sel_count, int max_sel, void* workspace, size_t ws_bytes,
                              void* stream);

@@ -15,6 +15,7 @@ struct oomb_pool {
   std::vector<int32_t> order;      // creation order of physical pages
   std::vector<int32_t> free_list;  // stack: back() is handed out next
   std::vector<int32_t> table;      // host copy of the page table
+  std::vector<int64_t> freed;      // logical pages freed since the last reset, ascending
   int64_t n_tokens = 0;
   int stage_buf = 0;
   bool table_dirty = true;  // device page table still needs its -1 fill
@@ -77,6 +78,7 @@ Geometry geometry_of(const oomb_pool_desc& d) {
 void rebuild_free_list(oomb_pool* p) {
   p->free_list.assign(p->order.rbegin(), p->order.rend());
   std::fill(p->table.begin(), p->table.end(), -1);
+  p->freed.clear();
   p->n_tokens = 0;
   p->table_dirty = true;
 }
@@ -289,6 +291,12 @@ oomb_status oomb_page_free(oomb_pool* p, int64_t first_logical_page, int n_pages
     p->free_list.push_back(p->table[i]);
     p->table[i] = -1;
   }
+  // appends map only new logical pages, so a freed logical page stays unmapped
+  std::vector<int64_t> add;
+  for (int64_t i = first_logical_page; i < end; ++i) add.push_back(i);
+  std::vector<int64_t> merged(p->freed.size() + add.size());
+  std::merge(p->freed.begin(), p->freed.end(), add.begin(), add.end(), merged.begin());
+  p->freed.swap(merged);
   return OOMB_OK;
 }
 
@@ -310,14 +318,21 @@ oomb_status oomb_page_select(oomb_pool* p, const void* q, int64_t q_start, int n
   const int64_t n_own = (q_start + n_q + P - 1) / P - n_hist;
   const int64_t sinks = n_sink < n_hist ? n_sink : n_hist;
   const int64_t cand = n_hist - sinks;
-  const int64_t kept = (top_k < 0 || cand <= top_k) ? cand : top_k;
-  if (sinks + kept + n_own > max_sel) return OOMB_ERR_ARG;
+  // freed pages are neither sinks nor candidates
+  auto n_freed = [p](int64_t lo, int64_t hi) {
+    return (int64_t)(std::lower_bound(p->freed.begin(), p->freed.end(), hi) -
+                     std::lower_bound(p->freed.begin(), p->freed.end(), lo));
+  };
+  const int64_t freed_sinks = n_freed(0, sinks), freed_cand = n_freed(sinks, n_hist);
+  const int64_t mapped = cand - freed_cand;
+  const int64_t kept = (top_k < 0 || mapped <= top_k) ? mapped : top_k;
+  if (sinks - freed_sinks + kept + n_own > max_sel) return OOMB_ERR_ARG;
   size_t need = select_workspace_bytes(p->g, n_q);
   if (!ws || ws_bytes < need) return OOMB_ERR_WORKSPACE;
   if (!aligned(ws, 16)) return OOMB_ERR_ALIGN;
-  return cuda_status(launch_page_select(p->g, p->d.summary, p->d.page_table, q, q_start, n_q, top_k, n_sink, sel,
-                                        sel_count, max_sel, ws, p->d.error_word, p->d.error_word,
-                                        (cudaStream_t)stream));
+  return cuda_status(launch_page_select(p->g, p->d.summary, p->d.page_table, q, q_start, n_q, top_k, n_sink,
+                                        (int)mapped, (freed_sinks + freed_cand) > 0 ? 1 : 0, sel, sel_count, max_sel,
+                                        ws, p->d.error_word, p->d.error_word, (cudaStream_t)stream));
 }
 
 oomb_status oomb_window_select(oomb_pool* p, int64_t q_start, int n_q, int window, int n_sink, int32_t* sel,

@@ -70,9 +70,12 @@ cudaError_t launch_kv_append(const Geometry& g, void* k_pool, void* v_pool, floa
                              cudaStream_t st);
 
 size_t select_workspace_bytes(const Geometry& g, int n_q);
+// n_mapped_cand: candidate pages [n_sink', q_start/P) whose table entry is mapped;
+// any_unmapped: some sink or candidate page is unmapped (freed) and must be skipped.
 cudaError_t launch_page_select(const Geometry& g, const float* summary, const int32_t* table, const void* q,
-                               int64_t q_start, int n_q, int top_k, int n_sink, int32_t* sel, int32_t* sel_count,
-                               int max_sel, void* ws, uint32_t* err, uint32_t* ctrl, cudaStream_t st);
+                               int64_t q_start, int n_q, int top_k, int n_sink, int n_mapped_cand, int any_unmapped,
+                               int32_t* sel, int32_t* sel_count, int max_sel, void* ws, uint32_t* err, uint32_t* ctrl,
+                               cudaStream_t st);
 
 // sel[h] = [0, sinks) U [lo, own_end) for every KV head h (host-validated bounds)
 cudaError_t launch_window_select(const Geometry& g, int sinks, int lo, int own_end, int32_t* sel,

@@ -62,6 +62,8 @@ struct SelParams {
   const float* summary;
   const int32_t* table;
   int n_sinks, cand0, n_cand, own0, n_own, top_k, max_sel;
+  int n_mapped_cand;    // candidates whose page is mapped (freed pages are not candidates)
+  int any_unmapped;     // some sink or candidate page is unmapped
   int pages_per_block;  // candidate pages scored by one CTA
   int half_pages;       // pages per shared-memory summary buffer (two buffers)
   uint32_t sum_off;     // byte offset of the summary buffers in dynamic shared memory
@@ -142,7 +144,7 @@ __device__ bool grid_sync(const SelParams& p, int i, bool wait) {
 // ------------------------------------------------------------------ phase 0
 // Bulk-copy the summary rows (Hkv * d fp32, contiguous per page) of pages
 // [first, first + n) of the candidates into buffer `buf`.  Called by warp 0.
-// An unmapped page is flagged and its row zero-filled (it then scores 0).
+// An unmapped (freed) page's row is zero-filled; it gets the lowest key in phase 3.
 __device__ void prefetch_summaries(const SelParams& p, uint8_t* smem, uint64_t* bar, int buf, int first, int n) {
   const int lane = threadIdx.x % 32;
   const uint32_t row_bytes = (uint32_t)(p.g.Hkv * p.g.d * 4);
@@ -162,7 +164,7 @@ __device__ void prefetch_summaries(const SelParams& p, uint8_t* smem, uint64_t* 
     if (phys >= 0 && phys < p.g.num_phys) {
       bulk_load(dst, p.summary + (size_t)phys * p.g.Hkv * p.g.d, row_bytes, bar);
     } else {
-      atomicOr(p.err, OOMB_DEVERR_PAGE);
+      if (phys >= p.g.num_phys) atomicOr(p.err, OOMB_DEVERR_PAGE);  // corrupt entry (-1 = freed)
       for (uint32_t b = 0; b < row_bytes; b += 16) *reinterpret_cast<uint4*>(dst + b) = make_uint4(0, 0, 0, 0);
     }
   }
@@ -328,8 +330,10 @@ __device__ bool page_scores(const SelParams& p, float* sh, uint64_t* sum_full, v
         }
         if (lane < 2 && (lane == 0 || it2 < n_items)) {
           const int i2 = lane == 0 ? it : it2;
-          const uint32_t key = order_key(lane == 0 ? s0 : s1);
           const int h = i2 % g.Hkv, j = j0 + first + i2 / g.Hkv;
+          // a mapped page's key is at least 1; an unmapped (freed) page's is 0, below all
+          uint32_t key = max(order_key(lane == 0 ? s0 : s1), 1u);
+          if (p.any_unmapped && __ldg(p.table + p.cand0 + j) < 0) key = 0u;
           p.keys[(size_t)h * p.key_stride + j] = key;
           atomicAdd(&p.hist[h * kHistBins + (key >> (32 - kHistBits))], 1u);
         }
@@ -397,14 +401,38 @@ __device__ void top_k_head(const SelParams& p, int h, uint32_t* sh_keys) {
   __shared__ int list_n, sh_bin, sh_krem, sh_kept, sh_need;
   __shared__ uint32_t sh_T;
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  __shared__ int sh_ns;
   const int n_cand = p.n_cand, top_k = p.top_k;
   int32_t* out = p.sel + (size_t)h * p.max_sel;
-  const bool take_all = (top_k < 0) || (n_cand <= top_k);
+  const bool take_all = (top_k < 0) || (p.n_mapped_cand <= top_k);
   const bool scored = !take_all && top_k > 0;
+  // the sink pages that are mapped (a freed page is no longer kept), in order
+  int ns = p.n_sinks;
+  if (p.any_unmapped) {
+    if (tid == 0) {
+      int c = 0;
+      for (int s = 0; s < p.n_sinks; ++s)
+        if (__ldg(p.table + s) >= 0) out[c++] = s;
+      sh_ns = c;
+    }
+    __syncthreads();
+    ns = sh_ns;
+  } else {
+    for (int s = tid; s < p.n_sinks; s += kThreads) out[s] = s;
+  }
   int kept = 0;
-  if (take_all) {
-    for (int i = tid; i < n_cand; i += kThreads) out[p.n_sinks + i] = p.cand0 + i;
+  if (take_all && !p.any_unmapped) {
+    for (int i = tid; i < n_cand; i += kThreads) out[ns + i] = p.cand0 + i;
     kept = n_cand;
+  } else if (take_all) {  // every mapped candidate, in page order
+    for (int base = 0; base < n_cand; base += kThreads) {
+      const int i = base + tid;
+      const int mapped = (i < n_cand && __ldg(p.table + p.cand0 + i) >= 0) ? 1 : 0;
+      int before;
+      const int total = block_exclusive_scan(mapped, &before, sh_warp);
+      if (mapped) out[ns + kept + before] = p.cand0 + i;
+      kept += total;
+    }
   } else if (scored) {
     const bool smem = p.keys_in_smem;
     const uint32_t* keys = p.keys + (size_t)h * p.key_stride;
@@ -592,7 +620,7 @@ __device__ void top_k_head(const SelParams& p, int h, uint32_t* sh_keys) {
     __syncthreads();
     // (5) ordered compaction
     const int need_eq = sh_need;
-    int pos = p.n_sinks + w_keep_before[warp], eq_rank = w_eq_before[warp];
+    int pos = ns + w_keep_before[warp], eq_rank = w_eq_before[warp];
     for (int base = i0; base < i1; base += 128) {
       const int i = base + 4 * lane;
       uint32_t u[4] = {0u, 0u, 0u, 0u};
@@ -630,9 +658,8 @@ __device__ void top_k_head(const SelParams& p, int h, uint32_t* sh_keys) {
     }
     kept = sh_kept;
   }
-  for (int s = tid; s < p.n_sinks; s += kThreads) out[s] = s;
-  for (int s = tid; s < p.n_own; s += kThreads) out[p.n_sinks + kept + s] = p.own0 + s;
-  if (tid == 0) p.sel_count[h] = p.n_sinks + kept + p.n_own;
+  for (int s = tid; s < p.n_own; s += kThreads) out[ns + kept + s] = p.own0 + s;
+  if (tid == 0) p.sel_count[h] = ns + kept + p.n_own;
   __syncthreads();  // shared memory is reused by the next head
 }
 
@@ -689,8 +716,9 @@ size_t select_workspace_bytes(const Geometry& g, int n_q) {
 }
 
 cudaError_t launch_page_select(const Geometry& g, const float* summary, const int32_t* table, const void* q,
-                               int64_t q_start, int n_q, int top_k, int n_sink, int32_t* sel, int32_t* sel_count,
-                               int max_sel, void* ws, uint32_t* err, uint32_t* ctrl, cudaStream_t st) {
+                               int64_t q_start, int n_q, int top_k, int n_sink, int n_mapped_cand, int any_unmapped,
+                               int32_t* sel, int32_t* sel_count, int max_sel, void* ws, uint32_t* err, uint32_t* ctrl,
+                               cudaStream_t st) {
   const size_t HD = (size_t)g.Hkv * g.d;
   char* w = (char*)ws;
   SelParams p;
@@ -719,7 +747,9 @@ cudaError_t launch_page_select(const Geometry& g, const float* summary, const in
   p.err = err;
   p.ctrl = ctrl;
   p.inv_count = 1.0f / ((float)n_q * g.G);
-  p.need_scores = p.n_cand > 0 && top_k > 0 && p.n_cand > top_k;
+  p.n_mapped_cand = n_mapped_cand;
+  p.any_unmapped = any_unmapped;
+  p.need_scores = p.n_cand > 0 && top_k > 0 && n_mapped_cand > top_k;
   p.keys_in_smem = p.n_cand <= kMaxSmemKeys;
   p.rows_per_block = 0;
   p.n_slices = 1;

@@ -472,3 +472,79 @@ def test_page_free_and_reuse():
     assert torch.equal(kk[w.seq:].cpu(), chunks[0]["k"]) and torch.equal(vv[w.seq:].cpu(), chunks[0]["v"])
     assert L.oomb_check(pool.handle) == 0
     pool.close()
+
+
+def test_select_skips_freed_pages():
+    """Freed pages (a sink and pages in the middle of the history) are never
+    selected: the top-K is taken over the mapped candidates only, a freed sink is
+    dropped, and "keep every candidate" keeps the mapped ones.  Expected: the
+    oracle's scores restricted to the mapped pages; the forward on the selection
+    then matches the oracle and raises no device error."""
+    w = synth.scaled(QWEN, "freed", seq=128 * 20, chunk=128 * 4, top_k=4, plants=2)
+    chunks, _ = make_chunks(w)
+    order = synth.page_order(w)
+    dev = torch.device("cuda")
+    pool = PagedKVPool(w.n_q_heads, w.n_kv_heads, w.head_dim, w.page, w.num_phys, w.n_pages, w.torch_dtype,
+                       dev, page_order=order)
+    opool = O.OraclePool(w.n_kv_heads, w.head_dim, w.page, w.num_phys, w.n_pages)
+    used = 0
+    for c, ch in enumerate(chunks):
+        start, n = w.chunk_bounds(c)
+        L.oomb_kv_append(pool.handle, ch["k"].to(dev), ch["v"].to(dev), start)
+        npg = -(-n // w.page)
+        opool.append(ch["k"].double().numpy(), ch["v"].double().numpy(), start, order[used:used + npg].tolist())
+        used += npg
+    c = w.n_chunks - 1
+    start, n = w.chunk_bounds(c)
+    qn = chunks[c]["q"].double().numpy()
+    q = chunks[c]["q"].to(dev)
+    freed = [0, 3, 4, 9]  # logical pages: one sink, three candidates
+    L.oomb_page_free(pool.handle, 0, 1)
+    L.oomb_page_free(pool.handle, 3, 2)
+    L.oomb_page_free(pool.handle, 9, 1)
+    n_hist = start // w.page
+    own = np.arange(n_hist, -(-(start + n) // w.page))
+    ws = pool.workspace(L.OOMB_OP_SELECT, w.chunk)
+    scale = 1.0 / math.sqrt(w.head_dim)
+    # 16 history pages; with two sinks 14 candidates, 11 of them mapped
+    for top_k, n_sink in [(4, 2), (10, 2), (11, 2), (12, 2), (-1, 2), (0, 1), (4, 0), (1, 3)]:
+        max_sel = w.n_pages + 4
+        sel = torch.full((w.n_kv_heads, max_sel), -1, dtype=torch.int32, device=dev)
+        cnt = torch.zeros(w.n_kv_heads, dtype=torch.int32, device=dev)
+        L.oomb_page_select(pool.handle, q, start, top_k, n_sink, sel, cnt, ws)
+        cand, scores = O.page_scores(opool, qn, start, n_sink)
+        keep = np.array([p not in freed for p in cand])
+        mcand, mscores = cand[keep], scores[:, keep]
+        sinks = np.array([p for p in range(min(n_sink, n_hist)) if p not in freed], dtype=np.int64)
+        exp = []
+        for h in range(w.n_kv_heads):
+            if top_k < 0 or mcand.size <= top_k:
+                chosen = mcand
+            else:
+                chosen = mcand[np.lexsort((mcand, -mscores[h]))[:top_k]]
+            exp.append(np.sort(np.concatenate([sinks, chosen, own]).astype(np.int64)))
+        got = [sel[h, : int(cnt[h])].cpu().numpy() for h in range(w.n_kv_heads)]
+        for h in range(w.n_kv_heads):
+            assert not set(got[h].tolist()) & set(freed), (top_k, n_sink, h, got[h])
+            assert np.all(np.diff(got[h]) > 0), "ascending"
+            ok, _ = O.near_tie_ok(got[h], exp[h], mcand, mscores[h], top_k)
+            assert ok, (top_k, n_sink, h, got[h], exp[h])
+        o = torch.empty_like(q)
+        lse = torch.empty(w.n_q_heads, n, dtype=torch.float32, device=dev)
+        L.oomb_chunk_attn_fwd(pool.handle, q, start, sel, cnt, scale, o, lse)
+        ro, rl = O.chunk_attn_fwd(opool, qn, start, got, scale)
+        assert O.rel_l2(f64(o), ro) < TOL[w.dtype] and O.rel_l2(f64(lse), rl) < TOL[w.dtype]
+        assert L.oomb_check(pool.handle) == 0, (top_k, n_sink)
+    # max_sel is checked against the mapped pages: 1 sink + 11 candidates + own fits exactly
+    fit = 1 + 11 + own.size
+    for slots, ok in [(fit, True), (fit - 1, False)]:
+        sel = torch.full((w.n_kv_heads, slots), -1, dtype=torch.int32, device=dev)
+        cnt = torch.zeros(w.n_kv_heads, dtype=torch.int32, device=dev)
+        if ok:
+            L.oomb_page_select(pool.handle, q, start, -1, 2, sel, cnt, ws)
+            assert cnt.cpu().tolist() == [fit] * w.n_kv_heads
+        else:
+            with pytest.raises(L.OombError):
+                L.oomb_page_select(pool.handle, q, start, -1, 2, sel, cnt, ws)
+    assert L.oomb_check(pool.handle) == 0
+    pool.close()
