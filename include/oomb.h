@@ -80,6 +80,7 @@ typedef enum { OOMB_OP_SELECT = 0, OOMB_OP_BWD = 1 } oomb_op;
 #define OOMB_DEVERR_PAGE 0x2u     /* page table entry unmapped / out of range */
 #define OOMB_DEVERR_SEL 0x4u      /* selection index out of range */
 #define OOMB_DEVERR_TMEM 0x8u     /* tensor-memory allocation failed */
+#define OOMB_DEVERR_SMEM 0x10u    /* a kernel's shared-memory window is not 1 KB aligned (nothing computed) */
 
 /* Length of the pool's control block (oomb_pool_desc.error_word), in uint32.
  * Word 0 holds the error bits above; words 4..5 are the grid-barrier counters of

@@ -52,7 +52,7 @@ namespace {
 
 using namespace tc;
 
-constexpr int kRing = 3;
+constexpr int kRing = 4;  // Q/dO half tiles in flight: the loads come from L2 and need the depth
 constexpr int kHalf = 64;
 constexpr uint32_t kHalfTile = kHalf * kD * 2;  // 16 KB: one 64-row half tile (two 8 KB boxes)
 constexpr uint32_t kHalfBox = kHalfTile / 2;
@@ -100,7 +100,10 @@ constexpr uint32_t kOffRing = kOffV + kTileBytes;                 // kRing x (Q 
 constexpr uint32_t kOffDS = kOffRing + kRing * 2 * kHalfTile;     // 2 x dS^T half [128 keys][64 q]
 constexpr uint32_t kOffVec = kOffDS + 2 * kHalfTile;              // kRing x (lse2[64], D[64])
 constexpr uint32_t kOffBar = kOffVec + kRing * 2 * kHalf * 4;
-constexpr size_t kSmemBytes = 1024 + kOffBar + sizeof(BwdBarriers);
+// No alignment slack: the kernel has no static shared memory, and its dynamic window
+// starts on a 1 KB boundary (checked at entry; the swizzled tiles need it).
+constexpr size_t kSmemBytes = kOffBar + sizeof(BwdBarriers);
+static_assert(kSmemBytes <= 232448, "shared memory budget");
 // Epilogue staging of a CTA's partial gradients, over the K/V tiles and the ring (all
 // MMAs have completed by then): [128 key rows][64 float4] = dV columns (float4 0..31)
 // then scale*dK (32..63), float4 c of row j stored at position c ^ (j & 7).
@@ -153,7 +156,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_steps = (int)((int64_t)all_steps * (part + 1) / p.n_split) - u0;
 
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  if (smem_u32(smem_raw) & 1023u) {  // uniform over the grid: every CTA leaves here
+    if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(p.err, OOMB_DEVERR_SMEM);
+    return;
+  }
+  uint8_t* sm = smem_raw;
   BwdBarriers* bar = reinterpret_cast<BwdBarriers*>(sm + kOffBar);
   float* vec = reinterpret_cast<float*>(sm + kOffVec);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
