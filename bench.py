@@ -152,6 +152,9 @@ class Step:
         # transfer blocks beside the attention CTAs at once, instead of after the last of
         # a long attention grid's pending blocks
         self.side = torch.cuda.Stream(device=dev, priority=-1) if self.offload else None
+        # the forward sweep's K/V write-backs (device -> host) run beside the gathers
+        # (host -> device) on a stream of their own: the link moves both directions at once
+        self.side_wb = torch.cuda.Stream(device=dev, priority=-1) if self.offload else None
 
     def run(self, record=False, no_recompute=False, wait_in=None, on_dq=None, on_fwd=None):
         """One step.  The reverse sweep recomputes each chunk's O and LSE (activations are
@@ -199,10 +202,13 @@ class Step:
         """K/V pools (and, with offload_grads, the fp32 dK/dV pools) in pinned host memory.
         The side stream moves the selected blocks of the next chunk into the other
         staging buffer while the main stream runs the current chunk's attention (forward
-        sweep: chunk c+1 is appended and selected before chunk c's forward; reverse sweep:
-        chunk c-1's K/V and the gradient blocks it does not share with chunk c are
-        staged during chunk c's backward; after it, the shared blocks are carried over
-        from chunk c's staging and chunk c's blocks are written back to the host)."""
+        sweep: chunk c+1 is selected and appended before chunk c's forward, the append
+        writing its pages into their staging slots only, and the side stream then
+        gathers chunk c+1's history pages and writes its own pages to the host pools;
+        reverse sweep: chunk c-1's K/V and the gradient blocks it does not share with
+        chunk c are staged during chunk c's backward; after it, the shared blocks are
+        carried over from chunk c's staging and chunk c's blocks are written back to the
+        host)."""
         L, w, h, torch = self.L, self.w, self.pool.handle, self.torch
         main, side = torch.cuda.current_stream(self.dev), self.side
         S = w.n_chunks
@@ -210,18 +216,41 @@ class Step:
         ev = lambda: torch.cuda.Event()  # noqa: E731
         L.oomb_pool_reset(h)
 
+        app_ev = {}
+
         def append_select(c):
-            """Selection (it needs the history only), then the append, which also writes
-            the chunk's own pages into their staging slots of buffer c % 2."""
+            """Selection (it needs the history only), then the append, which writes the
+            chunk's own pages into their staging slots of buffer c % 2 only."""
             start, n = w.chunk_bounds(c)
             ch = self.chunks[c]
             if wait_in is not None:
                 main.wait_event(wait_in[c])
             self._select(c, ch, start, n, record)
-            self._timed(record, self.app_events, c, L.oomb_kv_append_staged, h, ch["k"], ch["v"], start,
+            self._timed(record, self.app_events, c, L.oomb_kv_append_deferred, h, ch["k"], ch["v"], start,
                         self.cnt[c], w.max_sel, c % 2)
+            app_ev[c] = ev()
+            app_ev[c].record(main)
             if on_fwd is not None:
                 on_fwd(c)
+
+        side_wb = self.side_wb
+
+        def kv_writeback(c):
+            """Chunk c's own pages, appended into staging buffer c % 2, to the host pools,
+            on the write-back stream (every later gather waits for it)."""
+            side_wb.wait_event(app_ev[c])
+            start, n = w.chunk_bounds(c)
+            if record:
+                p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                p0.record(side_wb)
+            L.oomb_kv_writeback(h, self.sel[c], self.cnt[c], c % 2, start // w.page, -(-(start + n) // w.page),
+                                stream=side_wb)
+            if record:
+                p1.record(side_wb)
+                self.prefetch_events.append((p0, p1, c))
+            done = ev()
+            done.record(side_wb)
+            return done
 
         def side_timed(c, fn):
             if record:
@@ -257,24 +286,26 @@ class Step:
 
         # forward sweep (K/V only)
         append_select(0)
-        sel_ev = ev()
-        sel_ev.record(main)
-        pf = {0: prefetch(0, [sel_ev], prev=False)}
+        pf = {0: prefetch(0, [app_ev[0]], prev=False)}
+        wb = {0: kv_writeback(0)}
         used = {}
         for c in range(S):
             if c + 1 < S:
+                if c - 1 in wb:  # the append refills buffer (c + 1) % 2: chunk c-1's pages are on the host
+                    main.wait_event(wb[c - 1])
                 append_select(c + 1)
-                e = ev()
-                e.record(main)
-                pf[c + 1] = prefetch(c + 1, [e] + ([used[c - 1]] if c - 1 in used else []), prev=False)
+                # chunk c+1's history includes chunk c's pages: gathered after their write-back
+                pf[c + 1] = prefetch(c + 1, [app_ev[c + 1], wb[c]] + ([used[c - 1]] if c - 1 in used else []),
+                                     prev=False)
+                wb[c + 1] = kv_writeback(c + 1)
             main.wait_event(pf[c])
             L.oomb_pool_set_stage(h, c % 2)
             start, n = w.chunk_bounds(c)
             self._fwd(c, self.chunks[c], start, n, record)
             used[c] = ev()
             used[c].record(main)
-        # reverse sweep
-        ready = {S - 1: prefetch(S - 1, [used[S - 1]], prev=None)}
+        # reverse sweep (its gathers read every page from the host pools)
+        ready = {S - 1: prefetch(S - 1, [used[S - 1], wb[S - 1]], prev=None)}
         for c in range(S - 1, -1, -1):
             if c - 1 >= 0:  # buffer (c-1) % 2 was last used by chunk c+1 (or, first, the forward sweep)
                 ready[c - 1] = prefetch(c - 1, [used[c + 1]] if c + 1 < S else [used[S - 1]], prev=c)
@@ -297,6 +328,7 @@ class Step:
                     ready[c - 1].record(side)
                 side_timed(c, lambda: L.oomb_grad_writeback(h, self.sel[c], self.cnt[c], c % 2, stream=side))
         main.wait_stream(side)  # the last write-backs belong to the step
+        main.wait_stream(side_wb)
 
     def _timed(self, record, events, c, fn, *args):
         if not record:
@@ -902,8 +934,6 @@ def main():
     app_ref = same_size_gbs(max(app_b.values()), dev, "copy") if app_gbs else None
     sel_ref = same_size_gbs(max(sel_b.values()), dev, "read") if sel_gbs else None
     hbm_peak = peaks.get("hbm_gbs", 6783.0)
-    # with offload the append writes K/V into host memory: its bound is the host link
-    app_peak = None
     value = job_throughput(credited, ms, world) / 1e12
     tokens_per_s = job_throughput(w.seq, ms, world)
     rec_ms = sum(a.elapsed_time(b) for a, b, _ in step.recompute_events) / args.steps
@@ -931,7 +961,11 @@ def main():
         n_blk = [sum(len(x) for x in sets[c]) for c in range(S)]
         kv_blk = 2 * w.page * w.head_dim * esz   # K and V of one (page, KV head)
         g_blk = 2 * w.page * w.head_dim * 4      # dK and dV
-        kv_in = 2 * sum(n_blk) * kv_blk           # both sweeps
+        # forward sweep: the history blocks (the append stages the own pages, which the
+        # side stream then writes to the host pools); reverse sweep: every selected block
+        own_blk = [-(-w.chunk_bounds(c)[1] // w.page) * Hkv for c in range(S)]
+        kv_in = sum(2 * n_blk[c] - own_blk[c] for c in range(S)) * kv_blk
+        kv_out = sum(own_blk) * kv_blk
         g_in = g_out = carried = 0
         if step.offload_grads:
             for c in range(S):
@@ -939,7 +973,7 @@ def main():
                 g_in += (n_blk[c] - shared) * g_blk
                 carried += shared * g_blk
                 g_out += n_blk[c] * g_blk
-        link_b = kv_in + g_in + g_out
+        link_b = kv_in + kv_out + g_in + g_out
         pf_s = sum(a.elapsed_time(b) for a, b, _ in step.prefetch_events) * 1e-3 / args.steps
         # isolated: each of the last chunks' K/V gathers three times in a row (the first
         # gather of a page set after the step can take far longer than the repeats,
@@ -972,7 +1006,7 @@ def main():
         link = 4 * (256 << 20) / (c0.elapsed_time(c1) * 1e-3) / 1e9
         del hbuf, dbuf
         prefetch = {"link": "pinned host memory <-> HBM staging over NVLink-C2C (side stream, zero-copy kernels)",
-                    "host_bytes_per_step": {"kv_in": kv_in, "grad_in": g_in, "grad_out": g_out,
+                    "host_bytes_per_step": {"kv_in": kv_in, "kv_out": kv_out, "grad_in": g_in, "grad_out": g_out,
                                             "grad_carried_on_device": carried},
                     "gbs_overlapped": round(link_b / pf_s / 1e9, 1) if pf_s > 0 else None,
                     "gbs_isolated_kv_gather": round(statistics.median(iso), 1),
@@ -1008,12 +1042,9 @@ def main():
                          "traffic": recorded_traffic(w.name, "oomb_chunk_attn_bwd"),
                          "traffic_unit": "DRAM bytes per launch (ncu dram__bytes_read.sum + write.sum)"},
             "append_call": {"gbs": round(app_gbs, 1) if app_gbs else None,
-                            "frac_of_hbm": round(app_gbs / hbm_peak, 3) if app_gbs and not step.offload else None,
-                            "bound": "host link (K/V pools in pinned host memory)" if step.offload else "hbm",
-                            "host_write_gbs": (round(sum(w.chunk_bounds(c)[1] * w.n_kv_heads * w.head_dim * 2
-                                                         * (2 if w.dtype == "bf16" else 4) for _, _, c in step.app_events)
-                                                     / (sum(a.elapsed_time(b) for a, b, _ in step.app_events) * 1e-3)
-                                                     / 1e9, 1) if step.offload and step.app_events else None),
+                            "frac_of_hbm": round(app_gbs / hbm_peak, 3) if app_gbs else None,
+                            "bound": "hbm" + (" (offload: the pages go to their staging slots; the side stream "
+                                              "writes them to the host pools)" if step.offload else ""),
                             "same_size_copy_gbs": round(app_ref, 1) if app_ref else None,
                             "frac_of_same_size_copy": round(app_gbs / app_ref, 3) if app_ref else None,
                             "bytes_per_token_per_kv_head": 2 * 2 * w.head_dim * (2 if w.dtype == "bf16" else 4)

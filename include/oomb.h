@@ -155,6 +155,25 @@ OOMB_API oomb_status oomb_kv_append_staged(oomb_pool* pool, const void* k, const
                                            int n_tokens, const int32_t* sel_count, int max_sel, int stage_buf,
                                            void* stream);
 
+/* oomb_kv_append_staged without the host write: the new pages go to their staging
+ * slots only (plus the page table, summaries and grad_state, all in device memory),
+ * so the append on the critical path touches no host memory; the host pool blocks
+ * are written afterwards by oomb_kv_writeback, e.g. on the side stream while the
+ * chunk's forward runs (explainer 2.C: transfers hidden behind computation).  Until
+ * that write-back has run, the host pools do not hold the chunk's pages: order it
+ * before any oomb_prefetch / oomb_prefetch_pages that reads them, and before the
+ * staging slots are written again.  Errors: those of oomb_kv_append_staged. */
+OOMB_API oomb_status oomb_kv_append_deferred(oomb_pool* pool, const void* k, const void* v, int64_t first_token,
+                                             int n_tokens, const int32_t* sel_count, int max_sel, int stage_buf,
+                                             void* stream);
+
+/* The reverse of oomb_prefetch_pages: every selected block of a page in
+ * [first_page, end_page) is copied from staging buffer stage_buf to its block of
+ * the host K/V pools.  Used after oomb_kv_append_deferred with the chunk's own pages
+ * as the range.  Errors: ARG, UNSUPPORTED (not an offload pool), CUDA. */
+OOMB_API oomb_status oomb_kv_writeback(oomb_pool* pool, const int32_t* sel, const int32_t* sel_count, int max_sel,
+                                       int stage_buf, int64_t first_page, int64_t end_page, void* stream);
+
 /* Return logical pages [first_logical_page, first_logical_page + n_pages) to the
  * free list (explainer 2.B: fixed-size pages; "3. Key Contributions": paged
  * memory without fragmentation).  Every page of the range must be mapped (already

@@ -7,8 +7,8 @@ library (``build``) and draws seeded synthetic inputs (``synth``).
 """
 from ._lib import (OOMB_BF16, OOMB_FP32, OOMB_OP_BWD, OOMB_OP_SELECT, OombError, header_symbols,  # noqa: F401
                    load, oomb_bias_rope, oomb_check, oomb_chunk_attn_bwd, oomb_chunk_attn_fwd, oomb_gemm, oomb_grad_carry,
-                   oomb_grad_gather, oomb_grad_prefetch, oomb_grad_writeback, oomb_kv_append, oomb_kv_append_staged,
-                   oomb_launch_count,
+                   oomb_grad_gather, oomb_grad_prefetch, oomb_grad_writeback, oomb_kv_append, oomb_kv_append_deferred,
+                   oomb_kv_append_staged, oomb_kv_writeback, oomb_launch_count,
                    oomb_page_free, oomb_page_select, oomb_page_select_noalloc, oomb_page_table_host, oomb_pool_create,
                    oomb_pool_destroy, oomb_pool_free_pages, oomb_pool_reset, oomb_pool_set_stage, oomb_pool_tokens,
                    oomb_prefetch, oomb_prefetch_pages, oomb_uses_tensor_cores, oomb_window_select, oomb_workspace_size)

@@ -64,6 +64,8 @@ def load(path: str = LIB_PATH) -> C.CDLL:
         "oomb_pool_reset": (i32, [vp, vp]),
         "oomb_kv_append": (i32, [vp, vp, vp, i64, i32, vp]),
         "oomb_kv_append_staged": (i32, [vp, vp, vp, i64, i32, vp, i32, i32, vp]),
+        "oomb_kv_append_deferred": (i32, [vp, vp, vp, i64, i32, vp, i32, i32, vp]),
+        "oomb_kv_writeback": (i32, [vp, vp, vp, i32, i32, i64, i64, vp]),
         "oomb_page_select": (i32, [vp, vp, i64, i32, i32, i32, vp, vp, i32, vp, sz, vp]),
         "oomb_chunk_attn_fwd": (i32, [vp, vp, i64, i32, vp, vp, i32, f32, vp, vp, vp]),
         "oomb_chunk_attn_bwd": (i32, [vp, vp, vp, vp, vp, i64, i32, vp, vp, i32, f32, vp, vp, sz, vp]),
@@ -143,6 +145,19 @@ def oomb_kv_append_staged(pool: int, k, v, first_token: int, sel_count, max_sel:
     n = k.shape[0] if n_tokens is None else n_tokens
     _ok("oomb_kv_append_staged", load().oomb_kv_append_staged(pool, _ptr(k), _ptr(v), first_token, n, _ptr(sel_count),
                                                               max_sel, stage_buf, _stream(stream)))
+
+
+def oomb_kv_append_deferred(pool: int, k, v, first_token: int, sel_count, max_sel: int, stage_buf: int,
+                            n_tokens: Optional[int] = None, stream=None) -> None:
+    n = k.shape[0] if n_tokens is None else n_tokens
+    _ok("oomb_kv_append_deferred", load().oomb_kv_append_deferred(pool, _ptr(k), _ptr(v), first_token, n,
+                                                                  _ptr(sel_count), max_sel, stage_buf, _stream(stream)))
+
+
+def oomb_kv_writeback(pool: int, sel, sel_count, stage_buf: int, first_page: int, end_page: int,
+                      stream=None) -> None:
+    _ok("oomb_kv_writeback", load().oomb_kv_writeback(pool, _ptr(sel), _ptr(sel_count), sel.shape[-1], stage_buf,
+                                                      first_page, end_page, _stream(stream)))
 
 
 def oomb_page_select(pool: int, q, q_start: int, top_k: int, n_sink: int, sel, sel_count, workspace,

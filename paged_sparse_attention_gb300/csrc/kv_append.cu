@@ -35,6 +35,7 @@ struct StageTarget {
   void* v;
   const int32_t* sel_count;  // [Hkv]
   int stage_h0, stride, max_sel, n_own, first_own;  // first_own: own page index of new page 0
+  int skip_pool;  // 1: write the staging slots only; the host pool blocks are written later
 };
 
 template <typename T>
@@ -121,9 +122,11 @@ __global__ void __launch_bounds__(kAppendThreads)
       for (int u = 0; u < kRowsInFlight; ++u) {
         const int r = rb + u * n_rg;
         if (r < P) {
-          const size_t off = blk + (size_t)r * d + (size_t)c * VEC;
-          *reinterpret_cast<uint4*>(k_pool + off) = kr[u];
-          *reinterpret_cast<uint4*>(v_pool + off) = vr[u];
+          if (!stg.skip_pool) {
+            const size_t off = blk + (size_t)r * d + (size_t)c * VEC;
+            *reinterpret_cast<uint4*>(k_pool + off) = kr[u];
+            *reinterpret_cast<uint4*>(v_pool + off) = vr[u];
+          }
           if (sk) {
             const size_t so = (size_t)r * d + (size_t)c * VEC;
             *reinterpret_cast<uint4*>(sk + so) = kr[u];
@@ -172,6 +175,7 @@ cudaError_t launch_kv_append(const Geometry& g, void* k_pool, void* v_pool, floa
       stg.max_sel = stage->max_sel;
       stg.n_own = n_new;
       stg.first_own = base;
+      stg.skip_pool = stage->skip_pool;
     }
     dim3 grid(cnt, g.Hkv);
     if (g.dtype == OOMB_FP32) {

@@ -260,8 +260,10 @@ oomb_status oomb_kv_append(oomb_pool* p, const void* k, const void* v, int64_t f
   return kv_append_impl(p, k, v, first_token, n_tokens, nullptr, stream);
 }
 
-oomb_status oomb_kv_append_staged(oomb_pool* p, const void* k, const void* v, int64_t first_token, int n_tokens,
-                                  const int32_t* sel_count, int max_sel, int stage_buf, void* stream) {
+// Shared body of oomb_kv_append_staged and oomb_kv_append_deferred.
+static oomb_status kv_append_stage_impl(oomb_pool* p, const void* k, const void* v, int64_t first_token,
+                                        int n_tokens, const int32_t* sel_count, int max_sel, int stage_buf,
+                                        int skip_pool, void* stream) {
   if (!p || !sel_count || max_sel <= 0) return OOMB_ERR_ARG;
   if (!p->d.offload) return OOMB_ERR_UNSUPPORTED;
   if (stage_buf < 0 || stage_buf > 1 || max_sel > p->d.stage_max_sel) return OOMB_ERR_ARG;
@@ -273,7 +275,18 @@ oomb_status oomb_kv_append_staged(oomb_pool* p, const void* k, const void* v, in
   sa.stage_h0 = stage_buf * p->g.Hkv;
   sa.stride = p->d.stage_max_sel;
   sa.max_sel = max_sel;
+  sa.skip_pool = skip_pool;
   return kv_append_impl(p, k, v, first_token, n_tokens, &sa, stream);
+}
+
+oomb_status oomb_kv_append_staged(oomb_pool* p, const void* k, const void* v, int64_t first_token, int n_tokens,
+                                  const int32_t* sel_count, int max_sel, int stage_buf, void* stream) {
+  return kv_append_stage_impl(p, k, v, first_token, n_tokens, sel_count, max_sel, stage_buf, 0, stream);
+}
+
+oomb_status oomb_kv_append_deferred(oomb_pool* p, const void* k, const void* v, int64_t first_token, int n_tokens,
+                                    const int32_t* sel_count, int max_sel, int stage_buf, void* stream) {
+  return kv_append_stage_impl(p, k, v, first_token, n_tokens, sel_count, max_sel, stage_buf, 1, stream);
 }
 
 oomb_status oomb_page_free(oomb_pool* p, int64_t first_logical_page, int n_pages, void* stream) {
@@ -427,6 +440,17 @@ oomb_status oomb_prefetch_pages(oomb_pool* p, const int32_t* sel, const int32_t*
   return cuda_status(launch_prefetch(p->g, p->d.k_pool, p->d.v_pool, p->d.page_table, sel, sel_count, max_sel,
                                      p->d.stage_k, p->d.stage_v, stage_buf * p->g.Hkv, p->d.stage_max_sel, lo, hi,
                                      p->d.error_word, (cudaStream_t)stream));
+}
+
+oomb_status oomb_kv_writeback(oomb_pool* p, const int32_t* sel, const int32_t* sel_count, int max_sel,
+                              int stage_buf, int64_t first_page, int64_t end_page, void* stream) {
+  if (!p || !sel || !sel_count || max_sel <= 0 || first_page < 0 || end_page < first_page) return OOMB_ERR_ARG;
+  if (!p->d.offload) return OOMB_ERR_UNSUPPORTED;
+  if (stage_buf < 0 || stage_buf > 1 || max_sel > p->d.stage_max_sel) return OOMB_ERR_ARG;
+  const int lo = (int)std::min<int64_t>(first_page, INT32_MAX), hi = (int)std::min<int64_t>(end_page, INT32_MAX);
+  return cuda_status(launch_prefetch(p->g, p->d.k_pool, p->d.v_pool, p->d.page_table, sel, sel_count, max_sel,
+                                     p->d.stage_k, p->d.stage_v, stage_buf * p->g.Hkv, p->d.stage_max_sel, lo, hi,
+                                     p->d.error_word, (cudaStream_t)stream, 1));
 }
 
 oomb_status oomb_prefetch(oomb_pool* p, const int32_t* sel, const int32_t* sel_count, int max_sel, int stage_buf,

@@ -60,6 +60,7 @@ struct StageArgs {
   void* v;
   const int32_t* sel_count;
   int stage_h0, stride, max_sel;
+  int skip_pool;  // 1: the new pages go to the staging slots only (the host pools later)
 };
 
 // ---- launchers (return cudaGetLastError of the launch) ----
@@ -92,7 +93,7 @@ size_t bwd_tc_workspace_bytes(const Geometry& g, int n_q);
 cudaError_t launch_prefetch(const Geometry& g, const void* k_pool, const void* v_pool, const int32_t* table,
                             const int32_t* sel, const int32_t* sel_count, int max_sel, void* stage_k, void* stage_v,
                             int stage_h0, int stage_stride, int first_page, int end_page, uint32_t* err,
-                            cudaStream_t st);
+                            cudaStream_t st, int to_host = 0);
 
 // Gradient staging (offload mode with host-resident dK/dV pools).  mode 0: stage the
 // blocks of `sel` whose page is not in `prev` from the host pools; mode 1: copy the

@@ -17,7 +17,8 @@
 // block), and only a few SMs carry the long-latency host accesses, which slow the
 // other memory traffic of the SM they run on.
 //
-//   gather_pages  K/V: slot (buf, h, s) <- pool block (phi(sel[h][s]), h)
+//   gather_pages  K/V: slot (buf, h, s) <- pool block (phi(sel[h][s]), h), or the
+//                 reverse (to_host: a chunk's own pages appended into their slots only)
 //   grad_copy     fp32 dK/dV, mode
 //                   from host: slot (buf, h, s) <- pool block, for pages not in prev;
 //                              a block that no write-back has reached since its page
@@ -92,10 +93,10 @@ __device__ __forceinline__ int selected_phys(const Geometry& g, const int32_t* t
 // (phi(sel[h][s]), h), for every item of the chunk's selection whose logical page is in
 // [first_page, end_page).
 __global__ void __launch_bounds__(kCopyThreads, 8)
-    gather_pages(Geometry g, const uint8_t* __restrict__ k_pool, const uint8_t* __restrict__ v_pool,
+    gather_pages(Geometry g, uint8_t* __restrict__ k_pool, uint8_t* __restrict__ v_pool,
                  const int32_t* __restrict__ table, const int32_t* __restrict__ sel,
                  const int32_t* __restrict__ sel_count, int max_sel, uint8_t* __restrict__ stage_k,
-                 uint8_t* __restrict__ stage_v, int stage_h0, int stride, int first_page, int end_page,
+                 uint8_t* __restrict__ stage_v, int stage_h0, int stride, int first_page, int end_page, int to_host,
                  uint32_t* err) {
   const size_t bytes = (size_t)g.P * g.d * dtype_size(g.dtype);
   const int n_items = max_sel * g.Hkv * 2;
@@ -107,9 +108,10 @@ __global__ void __launch_bounds__(kCopyThreads, 8)
     int p;
     const int phys = selected_phys(g, table, sel, max_sel, h, s, &p, err);
     if (phys < 0) continue;
-    const uint8_t* src = (which == 0 ? k_pool : v_pool) + ((size_t)phys * g.Hkv + h) * bytes;
-    uint8_t* dst = (which == 0 ? stage_k : stage_v) + ((size_t)(stage_h0 + h) * stride + s) * bytes;
-    copy_block(reinterpret_cast<uint4*>(dst), reinterpret_cast<const uint4*>(src), (int)(bytes / 16));
+    uint8_t* pool = (which == 0 ? k_pool : v_pool) + ((size_t)phys * g.Hkv + h) * bytes;
+    uint8_t* slot = (which == 0 ? stage_k : stage_v) + ((size_t)(stage_h0 + h) * stride + s) * bytes;
+    if (to_host) copy_block(reinterpret_cast<uint4*>(pool), reinterpret_cast<const uint4*>(slot), (int)(bytes / 16));
+    else copy_block(reinterpret_cast<uint4*>(slot), reinterpret_cast<const uint4*>(pool), (int)(bytes / 16));
   }
 }
 
@@ -171,11 +173,12 @@ __global__ void __launch_bounds__(kCopyThreads, 8)
 cudaError_t launch_prefetch(const Geometry& g, const void* k_pool, const void* v_pool, const int32_t* table,
                             const int32_t* sel, const int32_t* sel_count, int max_sel, void* stage_k, void* stage_v,
                             int stage_h0, int stage_stride, int first_page, int end_page, uint32_t* err,
-                            cudaStream_t st) {
+                            cudaStream_t st, int to_host) {
   const int grid = std::min(max_sel * g.Hkv * 2, kGatherCtas);
-  gather_pages<<<grid, kCopyThreads, 0, st>>>(g, (const uint8_t*)k_pool, (const uint8_t*)v_pool, table, sel,
-                                              sel_count, max_sel, (uint8_t*)stage_k, (uint8_t*)stage_v, stage_h0,
-                                              stage_stride, first_page, end_page, err);
+  gather_pages<<<grid, kCopyThreads, 0, st>>>(g, (uint8_t*)const_cast<void*>(k_pool),
+                                              (uint8_t*)const_cast<void*>(v_pool), table, sel, sel_count, max_sel,
+                                              (uint8_t*)stage_k, (uint8_t*)stage_v, stage_h0, stage_stride,
+                                              first_page, end_page, to_host, err);
   count_launches(1);
   return cudaGetLastError();
 }

@@ -48,11 +48,14 @@ class GpuSweep:
     selections to the attention calls (the GPU selection is still computed and
     kept in ``gpu_sel``).  With ``offload`` the K/V pools live in pinned host
     memory and every chunk's selected pages are prefetched on a side stream into
-    the staging buffer of its parity before its attention calls."""
+    the staging buffer of its parity before its attention calls.  ``staged_append``:
+    the append also writes the chunk's own pages into their staging slots and only
+    the history pages are gathered; "deferred": the append writes the slots only and
+    the side stream writes the own pages to the host pools afterwards."""
 
     def __init__(self, w: synth.Workload, chunks, order, dev="cuda", sel_override=None, scale=None,
                  num_phys: Optional[int] = None, offload: bool = False, offload_grads: bool = False,
-                 staged_append: bool = False):
+                 staged_append=False):
         self.w = w
         self.dev = torch.device(dev)
         self.scale = 1.0 / math.sqrt(w.head_dim) if scale is None else scale
@@ -96,9 +99,12 @@ class GpuSweep:
             if sel_override is not None:
                 sel, cnt = pad_sel(sel_override[c], max_sel, self.dev)
             if staged_append:  # own pages into their staging slots; only the history comes from the host
-                L.oomb_kv_append_staged(h, g["k"], g["v"], start, cnt, max_sel, c % 2)
+                append = L.oomb_kv_append_deferred if staged_append == "deferred" else L.oomb_kv_append_staged
+                append(h, g["k"], g["v"], start, cnt, max_sel, c % 2)
                 side.wait_stream(main)
                 L.oomb_prefetch_pages(h, sel, cnt, c % 2, 0, start // w.page, stream=side)
+                if staged_append == "deferred":  # the own pages to the host pools
+                    L.oomb_kv_writeback(h, sel, cnt, c % 2, start // w.page, -(-(start + n) // w.page), stream=side)
                 main.wait_stream(side)
                 L.oomb_pool_set_stage(h, c % 2)
             else:

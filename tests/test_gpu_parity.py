@@ -196,8 +196,8 @@ def test_host_errors_on_gpu():
     pool.close()
 
 
-@pytest.mark.parametrize("grads,staged", [(False, False), (True, False), (True, True)],
-                         ids=["kv", "kv+grads", "kv+grads+staged-append"])
+@pytest.mark.parametrize("grads,staged", [(False, False), (True, False), (True, True), (True, "deferred")],
+                         ids=["kv", "kv+grads", "kv+grads+staged-append", "kv+grads+deferred-append"])
 @pytest.mark.parametrize("name", ["bf16_sparse", "fp32_sparse", "bf16_window"])
 def test_offload_matches_resident(name, grads, staged):
     """K/V pools (and with grads the fp32 dK/dV pools) in pinned host memory, the
@@ -208,7 +208,10 @@ def test_offload_matches_resident(name, grads, staged):
     thread blocks in a run-dependent order) -- and within tolerance of the oracle.
     With the staged append the selection comes first (it needs the history only), the
     append writes the chunk's own pages into their staging slots, and only the history
-    pages are gathered from the host."""
+    pages are gathered from the host; with the deferred append the append writes the
+    slots only and the own pages reach the host pools by the side stream's write-back
+    (the reverse sweep gathers them from there, and the host pools must equal the
+    resident pools)."""
     w = {**CASES, **WINDOW_CASES}[name]
     chunks, _ = make_chunks(w)
     order = synth.page_order(w).tolist()
@@ -227,6 +230,9 @@ def test_offload_matches_resident(name, grads, staged):
     for a, b in zip(off.gpu_sel, res.gpu_sel):
         for x, y in zip(a, b):
             assert np.array_equal(x, y)
+    ok, ov = off.pool.logical_kv(w.seq)
+    rk, rv = res.pool.logical_kv(w.seq)
+    assert torch.equal(ok, rk) and torch.equal(ov, rv)
     res.pool.close()
     off.pool.close()
 
