@@ -156,15 +156,19 @@ class Step:
         # (host -> device) on a stream of their own: the link moves both directions at once
         self.side_wb = torch.cuda.Stream(device=dev, priority=-1) if self.offload else None
 
-    def run(self, record=False, no_recompute=False, wait_in=None, on_dq=None, on_fwd=None):
+    def run(self, record=False, no_recompute=False, wait_in=None, on_dq=None, on_fwd=None, wait_do=None,
+            on_rev=None):
         """One step.  The reverse sweep recomputes each chunk's O and LSE (activations are
         not kept).  With no_recompute the forward sweep's outputs are kept per chunk and
         the reverse sweep only runs the backward (the variant without recomputation).
         wait_in[c]: an event the step waits for before it first reads chunk c's inputs;
         on_fwd(c): called once chunk c's append has been issued, on_dq(c): once chunk
-        c's dQ has been issued (end-to-end copies)."""
+        c's dQ has been issued, on_rev(c): when the reverse sweep reaches chunk c;
+        wait_do[c]: an event the step waits for before chunk c's backward reads its dO
+        (end-to-end copies)."""
         if self.offload:
-            return self.run_offload(record, wait_in=wait_in, on_dq=on_dq, on_fwd=on_fwd)
+            return self.run_offload(record, wait_in=wait_in, on_dq=on_dq, on_fwd=on_fwd, wait_do=wait_do,
+                                    on_rev=on_rev)
         L, w, h, torch = self.L, self.w, self.pool.handle, self.torch
         L.oomb_pool_reset(h)
         for c, ch in enumerate(self.chunks):
@@ -192,23 +196,27 @@ class Step:
             return
         for c in range(w.n_chunks - 1, -1, -1):
             start, n = w.chunk_bounds(c)
+            if on_rev is not None:
+                on_rev(c)
             if c < w.n_chunks - 1:  # activations are not kept; the last chunk's are still in the buffers
                 self._fwd(c, self.chunks[c], start, n, record, recompute=True)
+            if wait_do is not None:
+                torch.cuda.current_stream(self.dev).wait_event(wait_do[c])
             self._bwd(c, self.chunks[c], start, n, record)
             if on_dq is not None:
                 on_dq(c)
 
-    def run_offload(self, record=False, wait_in=None, on_dq=None, on_fwd=None):
+    def run_offload(self, record=False, wait_in=None, on_dq=None, on_fwd=None, wait_do=None, on_rev=None):
         """K/V pools (and, with offload_grads, the fp32 dK/dV pools) in pinned host memory.
         The side stream moves the selected blocks of the next chunk into the other
         staging buffer while the main stream runs the current chunk's attention (forward
         sweep: chunk c+1 is selected and appended before chunk c's forward, the append
-        writing its pages into their staging slots only, and the side stream then
-        gathers chunk c+1's history pages and writes its own pages to the host pools;
-        reverse sweep: chunk c-1's K/V and the gradient blocks it does not share with
-        chunk c are staged during chunk c's backward; after it, the shared blocks are
-        carried over from chunk c's staging and chunk c's blocks are written back to the
-        host)."""
+        writing its pages into their staging slots only; the side stream then gathers
+        chunk c+1's history pages while a second high-priority stream writes its own
+        pages to the host pools; reverse sweep: chunk c-1's K/V and the gradient blocks
+        it does not share with chunk c are staged during chunk c's backward; after it,
+        the shared blocks are carried over from chunk c's staging and, on the write-back
+        stream, chunk c's blocks are written back to the host)."""
         L, w, h, torch = self.L, self.w, self.pool.handle, self.torch
         main, side = torch.cuda.current_stream(self.dev), self.side
         S = w.n_chunks
@@ -304,16 +312,25 @@ class Step:
             self._fwd(c, self.chunks[c], start, n, record)
             used[c] = ev()
             used[c].record(main)
-        # reverse sweep (its gathers read every page from the host pools)
+        # reverse sweep (its gathers read every page from the host pools); gradient
+        # write-backs go on the write-back stream, beside the gathers
         ready = {S - 1: prefetch(S - 1, [used[S - 1], wb[S - 1]], prev=None)}
+        wbg = {}
         for c in range(S - 1, -1, -1):
-            if c - 1 >= 0:  # buffer (c-1) % 2 was last used by chunk c+1 (or, first, the forward sweep)
-                ready[c - 1] = prefetch(c - 1, [used[c + 1]] if c + 1 < S else [used[S - 1]], prev=c)
+            if c - 1 >= 0:
+                # buffer (c-1) % 2 was last used by chunk c+1 (its backward and its write-back,
+                # which also wrote host blocks this gather may read), or first by the forward sweep
+                after = ([used[c + 1]] + ([wbg[c + 1]] if c + 1 in wbg else [])) if c + 1 < S else [used[S - 1]]
+                ready[c - 1] = prefetch(c - 1, after, prev=c)
+            if on_rev is not None:
+                on_rev(c)
             main.wait_event(ready[c])
             L.oomb_pool_set_stage(h, c % 2)
             start, n = w.chunk_bounds(c)
             if c < S - 1:  # the last chunk's O and LSE are still in the buffers
                 self._fwd(c, self.chunks[c], start, n, record, recompute=True)
+            if wait_do is not None:
+                main.wait_event(wait_do[c])
             self._bwd(c, self.chunks[c], start, n, record)
             used[c] = ev()
             used[c].record(main)
@@ -326,7 +343,16 @@ class Step:
                                                                 self.cnt[c], (c - 1) % 2, stream=side))
                     ready[c - 1] = ev()
                     ready[c - 1].record(side)
-                side_timed(c, lambda: L.oomb_grad_writeback(h, self.sel[c], self.cnt[c], c % 2, stream=side))
+                side_wb.wait_event(used[c])
+                if record:
+                    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    p0.record(side_wb)
+                L.oomb_grad_writeback(h, self.sel[c], self.cnt[c], c % 2, stream=side_wb)
+                if record:
+                    p1.record(side_wb)
+                    self.prefetch_events.append((p0, p1, c))
+                wbg[c] = ev()
+                wbg[c].record(side_wb)
         main.wait_stream(side)  # the last write-backs belong to the step
         main.wait_stream(side_wb)
 
@@ -445,9 +471,10 @@ class StackStep:
     (its page set does not depend on its queries); a top-K layer's history pages move
     while the layer's K/V projection runs (a synthetic GEMM of the layer's chunk, model
     width 3584, that the selection does not wait for); the append writes the chunk's
-    own pages into their staging slots; in the reverse sweep every layer's K/V and
-    gradient blocks are staged one layer ahead.
-    One high-priority side stream carries every transfer."""
+    own pages into their staging slots only, and a second high-priority stream writes
+    them to the host pools; in the reverse sweep every layer's K/V and gradient blocks
+    are staged one layer ahead, and the gradient write-backs go on the write-back
+    stream.  One high-priority side stream carries the gathers."""
 
     def __init__(self, w, n_layers, dev, model_dim=3584):
         import torch
@@ -456,6 +483,7 @@ class StackStep:
         from paged_sparse_attention_gb300 import synth
         self.L, self.torch, self.w, self.dev = L, torch, w, dev
         self.side = torch.cuda.Stream(device=dev, priority=-1)
+        self.side_wb = torch.cuda.Stream(device=dev, priority=-1)  # K/V write-backs (device -> host)
         self.layers = []
         for layer in range(n_layers):
             st = Step(synth.stack_layer(w, layer), dev)
@@ -482,9 +510,10 @@ class StackStep:
 
     def run(self, record=False):
         L, w, torch = self.L, self.w, self.torch
-        main, side = torch.cuda.current_stream(self.dev), self.side
+        main, side, side_wb = torch.cuda.current_stream(self.dev), self.side, self.side_wb
         S, NL = w.n_chunks, len(self.layers)
         ev = lambda: torch.cuda.Event()  # noqa: E731
+        wb = {}  # (c, layer): the chunk's own pages are in the layer's host pools
 
         def mark():
             e = ev()
@@ -503,6 +532,8 @@ class StackStep:
             self._main(record, st._select, c, st.chunks[c], start, n, False)
             e = mark()
             side.wait_event(e)
+            if (c - 1, layer) in wb:  # the history includes the previous chunk's pages
+                side.wait_event(wb[(c - 1, layer)])
             L.oomb_prefetch_pages(st.pool.handle, st.sel[c], st.cnt[c], c % 2, 0, start // w.page, stream=side)
             staged[(c, layer)] = True
 
@@ -517,10 +548,18 @@ class StackStep:
                 if self.layers[l2].w.window >= 0 and (c2, l2) not in staged:
                     select_and_stage(c2, l2)
             # the layer's K/V projection (synthetic) overlaps the history transfer; the
-            # append writes the chunk's own pages into their staging slots as well
+            # append writes the chunk's own pages into their staging slots only, and the
+            # write-back stream copies them to the host pools
             self._main(record, L.oomb_gemm, self.X[:n], self.Wkv, self.kv_acc[:n], workspace=self.gemm_ws)
-            self._main(record, L.oomb_kv_append_staged, h, st.chunks[c]["k"], st.chunks[c]["v"], start, st.cnt[c],
-                       st.w.max_sel, c % 2)
+            if (c - 2, layer) in wb:  # buffer c % 2 of this layer: chunk c-2's pages are on the host
+                main.wait_event(wb[(c - 2, layer)])
+            self._main(record, L.oomb_kv_append_deferred, h, st.chunks[c]["k"], st.chunks[c]["v"], start,
+                       st.cnt[c], st.w.max_sel, c % 2)
+            side_wb.wait_event(mark())
+            L.oomb_kv_writeback(h, st.sel[c], st.cnt[c], c % 2, start // w.page, -(-(start + n) // w.page),
+                                stream=side_wb)
+            wb[(c, layer)] = ev()
+            wb[(c, layer)].record(side_wb)
             done = ev()
             done.record(side)  # every history transfer issued so far, this item's included
             main.wait_event(done)
@@ -529,14 +568,16 @@ class StackStep:
                        st.ob[0][:n], st.lseb[0] if n == w.chunk else st.lse_tail(n))
         # reverse sweep: every item's K/V and gradient blocks staged one item ahead
         ritems = items[::-1]
-        bwd_done, ready = {}, {}
+        bwd_done, ready, wbg = {}, {}, {}
 
         def stage_rev(c, layer):
             st = self.layers[layer]
             h = st.pool.handle
             prev = c + 1 if c + 1 < S else None
-            if prev is not None:  # the carried blocks and the host blocks written back after it
+            if prev is not None:  # the carried blocks, and the host blocks written back after it
                 side.wait_event(bwd_done[(prev, layer)])
+                if (prev, layer) in wbg:
+                    side.wait_event(wbg[(prev, layer)])
             L.oomb_prefetch(h, st.sel[c], st.cnt[c], c % 2, stream=side)
             L.oomb_grad_prefetch(h, st.sel[c], st.cnt[c], st.sel[prev] if prev is not None else None,
                                  st.cnt[prev] if prev is not None else None, c % 2, stream=side)
@@ -547,6 +588,7 @@ class StackStep:
             ready[(c, layer)] = r
 
         side.wait_stream(main)  # the forward sweep's last reads of the staging buffers
+        side.wait_stream(side_wb)  # and its write-backs: the reverse sweep gathers every page from the host
         stage_rev(*ritems[0])
         for i, (c, layer) in enumerate(ritems):
             st = self.layers[layer]
@@ -566,9 +608,12 @@ class StackStep:
             self._main(record, L.oomb_chunk_attn_bwd, h, st.chunks[c]["q"], st.ob[0][:n], st.chunks[c]["do"], lse,
                        start, st.sel[c], st.cnt[c], st.scale, st.dq[c], st.ws_bwd)
             bwd_done[(c, layer)] = mark()
-            side.wait_event(bwd_done[(c, layer)])
-            L.oomb_grad_writeback(h, st.sel[c], st.cnt[c], c % 2, stream=side)
+            side_wb.wait_event(bwd_done[(c, layer)])
+            L.oomb_grad_writeback(h, st.sel[c], st.cnt[c], c % 2, stream=side_wb)
+            wbg[(c, layer)] = ev()
+            wbg[(c, layer)].record(side_wb)
         main.wait_stream(side)
+        main.wait_stream(side_wb)
 
     def pairs(self):
         return [sum(st.pairs_per_chunk()) for st in self.layers]
@@ -1139,29 +1184,43 @@ def measure_e2e(step, steps, credited, world, dev):
     copy = torch.cuda.Stream(device=dev)
     S = len(step.chunks)
 
+    fwd_keys = [k for k in step.chunks[0] if k != "do"]
+
     def one_step():
         copy.wait_stream(main)  # the previous step has finished reading the input buffers
-        ready = {}
+        ready, ready_do = {}, {}
 
-        def upload(c):
+        def upload(c, keys, done):
             with torch.cuda.stream(copy):
-                for k in step.chunks[c]:
+                for k in keys:
                     step.chunks[c][k].copy_(host_in[c][k], non_blocking=True)
-                ready[c] = torch.cuda.Event()
-                ready[c].record(copy)
+                done[c] = torch.cuda.Event()
+                done[c].record(copy)
 
-        # paced: chunk c + AHEAD is uploaded once chunk c's append has been issued, so
-        # that the uploads spread over the forward sweep instead of taking the host
-        # link in one burst (the offload gathers share it)
+        def after_main():
+            e = torch.cuda.Event()
+            e.record(main)
+            copy.wait_event(e)
+
+        # paced, each input when it is needed: Q, K, V of chunk c + AHEAD once chunk c's
+        # append has been issued (the uploads spread over the forward sweep instead of
+        # taking the host link in one burst; the offload gathers share it), and dO, which
+        # only the backward reads, AHEAD chunks ahead in the reverse sweep
         for c in range(min(E2E_AHEAD, S)):
-            upload(c)
+            upload(c, fwd_keys, ready)
 
         def on_fwd(c):
             if c + E2E_AHEAD < S:
-                e = torch.cuda.Event()
-                e.record(main)
-                copy.wait_event(e)
-                upload(c + E2E_AHEAD)
+                after_main()
+                upload(c + E2E_AHEAD, fwd_keys, ready)
+
+        def on_rev(c):
+            if c == S - 1:
+                for c2 in range(S - 1, max(-1, S - 1 - E2E_AHEAD), -1):
+                    upload(c2, ["do"], ready_do)
+            elif c - E2E_AHEAD + 1 >= 0:
+                after_main()
+                upload(c - E2E_AHEAD + 1, ["do"], ready_do)
 
         def on_dq(c):
             done = torch.cuda.Event()
@@ -1170,7 +1229,7 @@ def measure_e2e(step, steps, credited, world, dev):
             with torch.cuda.stream(copy):
                 host_dq[c].copy_(step.dq[c], non_blocking=True)
 
-        step.run(wait_in=ready, on_dq=on_dq, on_fwd=on_fwd)
+        step.run(wait_in=ready, on_dq=on_dq, on_fwd=on_fwd, wait_do=ready_do, on_rev=on_rev)
         if pools_on_device:
             copy.wait_stream(main)
             with torch.cuda.stream(copy):
@@ -1193,9 +1252,11 @@ def measure_e2e(step, steps, credited, world, dev):
         hp.close()
     return {"value": round(credited / (ms * 1e-3) / 1e12 * world, 3), "unit": UNIT, "ms_per_step": round(ms, 3),
             "ms_per_step_min_max": [round(min(per_step), 3), round(max(per_step), 3)],
+            "ms_each_step": [round(x, 2) for x in per_step],
             "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
-            "overlap": f"uploads per chunk on a copy stream, {E2E_AHEAD} chunks ahead of the forward sweep; "
-                       "dQ read back as each backward is issued"}
+            "overlap": f"uploads per chunk on a copy stream: Q, K, V {E2E_AHEAD} chunks ahead of the forward "
+                       f"sweep, dO {E2E_AHEAD} chunks ahead of the reverse sweep; dQ read back as each backward "
+                       "is issued"}
 
 
 if __name__ == "__main__":
