@@ -705,6 +705,45 @@ def config_of(w, world: int) -> dict:
             "attention_kernels": "tcgen05" if tc else "simt"}
 
 
+def host_link_bytes(w, sel, cnt, offload_grads: bool) -> dict:
+    """Bytes the offload step moves over the host link per step, from the selections
+    sel [S, Hkv, max_sel] and counts cnt [S, Hkv] (host arrays).  Forward sweep: each
+    chunk's history blocks are gathered (its own pages are appended into their staging
+    slots) and its own pages are written to the host pools; reverse sweep: every
+    selected K/V block is gathered.  Gradients (offload_grads): every selected block
+    is written back after its chunk's backward; a block of chunk c also selected by
+    chunk c+1 is carried over on the device; any other is read from the host only if
+    a chunk after c has written it back in this sweep (otherwise it is zero-filled on
+    the device: the append marked it empty)."""
+    S, Hkv = w.n_chunks, w.n_kv_heads
+    esz = 2 if w.dtype == "bf16" else 4
+    kv_blk = 2 * w.page * w.head_dim * esz   # K and V of one (page, KV head)
+    g_blk = 2 * w.page * w.head_dim * 4      # dK and dV
+    sets = [[set(int(x) for x in sel[c, hk, : int(cnt[c, hk])]) for hk in range(Hkv)] for c in range(S)]
+    kv_in = kv_out = g_in = g_out = carried = 0
+    for c in range(S):
+        first_own = w.chunk_bounds(c)[0] // w.page
+        for hk in range(Hkv):
+            hist = sum(1 for p in sets[c][hk] if p < first_own)
+            own = len(sets[c][hk]) - hist
+            kv_in += (hist + len(sets[c][hk])) * kv_blk
+            kv_out += own * kv_blk
+    if offload_grads:
+        for hk in range(Hkv):
+            written = set()
+            for c in range(S - 1, -1, -1):
+                nxt = sets[c + 1][hk] if c + 1 < S else set()
+                for p in sets[c][hk]:
+                    if p in nxt:
+                        carried += g_blk
+                    elif p in written:
+                        g_in += g_blk
+                g_out += len(sets[c][hk]) * g_blk
+                written |= sets[c][hk]
+    return {"kv_in": kv_in, "kv_out": kv_out, "grad_in": g_in, "grad_out": g_out,
+            "grad_carried_on_device": carried}
+
+
 def recorded_traffic(workload: str, kernel: str):
     """DRAM bytes per launch of `kernel` from an ncu capture recorded in
     profiles/traffic.txt, or None when there is none for this workload or the
@@ -998,27 +1037,11 @@ def main():
                   for a, b, _ in ev) / args.steps
     prefetch = None
     if step.offload:
-        import numpy as np
-        esz = 2 if w.dtype == "bf16" else 4
-        S, Hkv = w.n_chunks, w.n_kv_heads
-        sel_h, cnt_h = step.sel.cpu().numpy(), step.cnt.cpu().numpy()
-        sets = [[set(sel_h[c, hk, : int(cnt_h[c, hk])].tolist()) for hk in range(Hkv)] for c in range(S)]
-        n_blk = [sum(len(x) for x in sets[c]) for c in range(S)]
-        kv_blk = 2 * w.page * w.head_dim * esz   # K and V of one (page, KV head)
-        g_blk = 2 * w.page * w.head_dim * 4      # dK and dV
-        # forward sweep: the history blocks (the append stages the own pages, which the
-        # side stream then writes to the host pools); reverse sweep: every selected block
-        own_blk = [-(-w.chunk_bounds(c)[1] // w.page) * Hkv for c in range(S)]
-        kv_in = sum(2 * n_blk[c] - own_blk[c] for c in range(S)) * kv_blk
-        kv_out = sum(own_blk) * kv_blk
-        g_in = g_out = carried = 0
-        if step.offload_grads:
-            for c in range(S):
-                shared = sum(len(sets[c][hk] & sets[c + 1][hk]) for hk in range(Hkv)) if c + 1 < S else 0
-                g_in += (n_blk[c] - shared) * g_blk
-                carried += shared * g_blk
-                g_out += n_blk[c] * g_blk
-        link_b = kv_in + kv_out + g_in + g_out
+        S = w.n_chunks
+        hb = host_link_bytes(w, step.sel.cpu().numpy(), step.cnt.cpu().numpy(), step.offload_grads)
+        n_blk = [int(step.cnt[c].sum()) for c in range(S)]
+        kv_blk = 2 * w.page * w.head_dim * (2 if w.dtype == "bf16" else 4)
+        link_b = hb["kv_in"] + hb["kv_out"] + hb["grad_in"] + hb["grad_out"]
         pf_s = sum(a.elapsed_time(b) for a, b, _ in step.prefetch_events) * 1e-3 / args.steps
         # isolated: each of the last chunks' K/V gathers three times in a row (the first
         # gather of a page set after the step can take far longer than the repeats,
@@ -1051,8 +1074,7 @@ def main():
         link = 4 * (256 << 20) / (c0.elapsed_time(c1) * 1e-3) / 1e9
         del hbuf, dbuf
         prefetch = {"link": "pinned host memory <-> HBM staging over NVLink-C2C (side stream, zero-copy kernels)",
-                    "host_bytes_per_step": {"kv_in": kv_in, "kv_out": kv_out, "grad_in": g_in, "grad_out": g_out,
-                                            "grad_carried_on_device": carried},
+                    "host_bytes_per_step": hb,
                     "gbs_overlapped": round(link_b / pf_s / 1e9, 1) if pf_s > 0 else None,
                     "gbs_isolated_kv_gather": round(statistics.median(iso), 1),
                     "isolated_first_call_ms": first_ms,

@@ -55,6 +55,25 @@ def test_pool_create_validation(lib):
     assert lib.oomb_pool_create(C.byref(_desc(offload=1)), C.byref(h)) == 1  # no staging buffers
 
 
+def test_offload_pool_host_checks(lib):
+    """An offload pool (staging buffers given): the stage buffer index and max_sel
+    against the staging capacity are checked before any device work."""
+    h = C.c_void_p()
+    d = _desc(offload=1, stage_max_sel=8, stage_k=1 << 26, stage_v=1 << 27)
+    assert lib.oomb_pool_create(C.byref(d), C.byref(h)) == 0
+    pool = h.value
+    fake = 1 << 24
+    for fn in (lib.oomb_kv_append_staged, lib.oomb_kv_append_deferred):
+        assert fn(pool, fake, fake, 0, 128, fake, 8, 2, None) == 1  # stage buffer 2
+        assert fn(pool, fake, fake, 0, 128, fake, 9, 0, None) == 1  # max_sel above the staging capacity
+        assert fn(pool, fake, fake, 0, 128, fake + 2, 8, 0, None) == 3  # misaligned counts
+    assert lib.oomb_kv_writeback(pool, fake, fake, 8, 2, 0, 1, None) == 1
+    assert lib.oomb_kv_writeback(pool, fake, fake, 9, 0, 0, 1, None) == 1
+    assert lib.oomb_prefetch_pages(pool, fake, fake, 8, 0, 3, 2, None) == 1
+    assert lib.oomb_pool_free_pages(pool) == 4  # nothing was taken
+    lib.oomb_pool_destroy(pool)
+
+
 def test_allocator_host_logic(lib):
     order = (C.c_int32 * 4)(2, 0, 3, 1)
     h = C.c_void_p()
@@ -79,6 +98,12 @@ def test_allocator_host_logic(lib):
     assert lib.oomb_window_select(pool, 0, 128, -1, 1, fake, fake, 8, None) == 1  # negative window
     assert lib.oomb_window_select(pool, 64, 128, 2, 1, fake, fake, 8, None) == 3  # start not on a page
     assert lib.oomb_prefetch(pool, fake, fake, 8, 0, None) == 8  # not an offload pool
+    # the staged and deferred appends and the K/V write-back need an offload pool
+    assert lib.oomb_kv_append_staged(pool, fake, fake, 0, 128, fake, 8, 0, None) == 8
+    assert lib.oomb_kv_append_deferred(pool, fake, fake, 0, 128, fake, 8, 0, None) == 8
+    assert lib.oomb_kv_writeback(pool, fake, fake, 8, 0, 0, 1, None) == 8
+    assert lib.oomb_kv_writeback(pool, fake, fake, 8, 0, 2, 1, None) == 1  # end before start
+    assert lib.oomb_kv_writeback(pool, None, fake, 8, 0, 0, 1, None) == 1
     assert lib.oomb_pool_set_stage(pool, 0) == 8
     assert lib.oomb_workspace_size(pool, 0, 4096) > 0
     assert lib.oomb_workspace_size(pool, 1, 4096) >= 28 * 4096 * 4

@@ -105,3 +105,27 @@ def test_algorithmic_bytes_per_call():
     assert off["fixed_staging_device"] == 2 * Hkv * w4.max_sel * P * d * (2 * 2 + 2 * 4)
     kv_only = bench.state_bytes_per_10k(synth.scaled(w4, "kv_only", offload_grads=False))
     assert kv_only["host"] == 10_000 * Hkv * d * 2 * 2 and kv_only["device"] == st["device"] - kv_only["host"]
+
+
+def test_host_link_bytes_hand_example():
+    """The offload step's host-link bytes on a 3-chunk, 1-head example worked by hand:
+    chunk 0 selects pages {0, 1} (own), chunk 1 {0 | 2, 3}, chunk 2 {1, 3 | 4, 5}.
+    K/V: forward gathers 0 + 1 + 2 history blocks, reverse gathers 2 + 3 + 4, own pages
+    written back 2 + 2 + 2.  Gradients, reverse order: chunk 2 zero-fills all four and
+    writes them back; chunk 1 carries page 3, zero-fills 0 and 2 (never written back);
+    chunk 0 carries page 0 and reads page 1 from the host (written back by chunk 2)."""
+    w = synth.scaled(synth.WORKLOADS["tiny"], "link", n_q_heads=1, n_kv_heads=1, head_dim=64, page=128, seq=768,
+                     chunk=256, top_k=-1, plants=0)
+    sel = np.full((3, 1, 4), -1, dtype=np.int32)
+    cnt = np.zeros((3, 1), dtype=np.int32)
+    for c, pages in enumerate([[0, 1], [0, 2, 3], [1, 3, 4, 5]]):
+        sel[c, 0, : len(pages)] = pages
+        cnt[c, 0] = len(pages)
+    esz = 2 if w.dtype == "bf16" else 4
+    kv_blk, g_blk = 2 * 128 * 64 * esz, 2 * 128 * 64 * 4
+    got = bench.host_link_bytes(w, sel, cnt, True)
+    assert got == {"kv_in": 12 * kv_blk, "kv_out": 6 * kv_blk, "grad_in": 1 * g_blk, "grad_out": 9 * g_blk,
+                   "grad_carried_on_device": 2 * g_blk}
+    no_grads = bench.host_link_bytes(w, sel, cnt, False)
+    assert no_grads["grad_in"] == no_grads["grad_out"] == no_grads["grad_carried_on_device"] == 0
+    assert no_grads["kv_in"] == 12 * kv_blk and no_grads["kv_out"] == 6 * kv_blk
