@@ -18,6 +18,7 @@ exchange step); `value` sums all ranks.
 from __future__ import annotations
 
 import argparse
+import gc
 import json
 import math
 import os
@@ -641,11 +642,12 @@ def run_stack(args, w, world, dev):
     with ClockSampler(0 if not torch.cuda.is_available() else torch.cuda.current_device()) as clk:
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(args.steps):
-            stack.run(record=True)
-        e1.record()
-        torch.cuda.synchronize()
+        with gc_paused():
+            e0.record()
+            for _ in range(args.steps):
+                stack.run(record=True)
+            e1.record()
+            torch.cuda.synchronize()
     launches = L.oomb_launch_count() - launches0
     ms = reduce_max_ms(e0.elapsed_time(e1) / args.steps, world, dev)
     for st in stack.layers:
@@ -742,6 +744,24 @@ def host_link_bytes(w, sel, cnt, offload_grads: bool) -> dict:
                 written |= sets[c][hk]
     return {"kv_in": kv_in, "kv_out": kv_out, "grad_in": g_in, "grad_out": g_out,
             "grad_carried_on_device": carried}
+
+
+class gc_paused:
+    """Python's cyclic garbage collector held off inside a timed region (reference
+    counting still frees everything the steps drop): the host thread that issues a
+    step's thousands of calls and events would otherwise stop for a full collection
+    now and then, which shows as a stray slow step when the GPU waits on the host."""
+
+    def __enter__(self):
+        gc.collect()
+        self.was = gc.isenabled()
+        gc.disable()
+        return self
+
+    def __exit__(self, *exc):
+        if self.was:
+            gc.enable()
+        return False
 
 
 def recorded_traffic(workload: str, kernel: str):
@@ -974,11 +994,12 @@ def main():
         torch.cuda.synchronize()
         torch.cuda.nvtx.range_push("oomb_timed_steps")  # the profiler's launch list filters on it
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(args.steps):
-            step.run(record=True)
-        e1.record()
-        torch.cuda.synchronize()
+        with gc_paused():
+            e0.record()
+            for _ in range(args.steps):
+                step.run(record=True)
+            e1.record()
+            torch.cuda.synchronize()
         torch.cuda.nvtx.range_pop()
         barrier()
     launches = L.oomb_launch_count() - launches0
@@ -1262,11 +1283,12 @@ def measure_e2e(step, steps, credited, world, dev):
     one_step()  # warm-up of the copy path
     torch.cuda.synchronize()
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
-    ev[0].record()
-    for i in range(steps):
-        one_step()
-        ev[i + 1].record()
-    torch.cuda.synchronize()
+    with gc_paused():
+        ev[0].record()
+        for i in range(steps):
+            one_step()
+            ev[i + 1].record()
+        torch.cuda.synchronize()
     per_step = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
     ms = ev[0].elapsed_time(ev[steps]) / steps
     hb.close()
