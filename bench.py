@@ -169,7 +169,7 @@ class Step:
         (end-to-end copies)."""
         if self.offload:
             return self.run_offload(record, wait_in=wait_in, on_dq=on_dq, on_fwd=on_fwd, wait_do=wait_do,
-                                    on_rev=on_rev)
+                                    on_rev=on_rev, no_recompute=no_recompute)
         L, w, h, torch = self.L, self.w, self.pool.handle, self.torch
         L.oomb_pool_reset(h)
         for c, ch in enumerate(self.chunks):
@@ -181,11 +181,7 @@ class Step:
                 on_fwd(c)
             self._select(c, ch, start, n, record)
             if no_recompute:
-                if c not in self.o_keep:
-                    self.o_keep[c] = torch.empty_like(ch["q"])
-                    self.lse_keep[c] = torch.empty((w.n_q_heads, n), dtype=torch.float32, device=self.dev)
-                L.oomb_chunk_attn_fwd(h, ch["q"], start, self.sel[c], self.cnt[c], self.scale, self.o_keep[c],
-                                      self.lse_keep[c])
+                self._fwd_keep(c, ch, start, n)
             else:
                 self._fwd(c, ch, start, n, record)
         if no_recompute:
@@ -207,7 +203,8 @@ class Step:
             if on_dq is not None:
                 on_dq(c)
 
-    def run_offload(self, record=False, wait_in=None, on_dq=None, on_fwd=None, wait_do=None, on_rev=None):
+    def run_offload(self, record=False, wait_in=None, on_dq=None, on_fwd=None, wait_do=None, on_rev=None,
+                    no_recompute=False):
         """K/V pools (and, with offload_grads, the fp32 dK/dV pools) in pinned host memory.
         The side stream moves the selected blocks of the next chunk into the other
         staging buffer while the main stream runs the current chunk's attention (forward
@@ -310,7 +307,10 @@ class Step:
             main.wait_event(pf[c])
             L.oomb_pool_set_stage(h, c % 2)
             start, n = w.chunk_bounds(c)
-            self._fwd(c, self.chunks[c], start, n, record)
+            if no_recompute:  # the forward sweep's outputs kept per chunk for the backward
+                self._fwd_keep(c, self.chunks[c], start, n)
+            else:
+                self._fwd(c, self.chunks[c], start, n, record)
             used[c] = ev()
             used[c].record(main)
         # reverse sweep (its gathers read every page from the host pools); gradient
@@ -328,11 +328,16 @@ class Step:
             main.wait_event(ready[c])
             L.oomb_pool_set_stage(h, c % 2)
             start, n = w.chunk_bounds(c)
-            if c < S - 1:  # the last chunk's O and LSE are still in the buffers
-                self._fwd(c, self.chunks[c], start, n, record, recompute=True)
-            if wait_do is not None:
-                main.wait_event(wait_do[c])
-            self._bwd(c, self.chunks[c], start, n, record)
+            if no_recompute:
+                ch = self.chunks[c]
+                L.oomb_chunk_attn_bwd(h, ch["q"], self.o_keep[c], ch["do"], self.lse_keep[c], start, self.sel[c],
+                                      self.cnt[c], self.scale, self.dq[c], self.ws_bwd)
+            else:
+                if c < S - 1:  # the last chunk's O and LSE are still in the buffers
+                    self._fwd(c, self.chunks[c], start, n, record, recompute=True)
+                if wait_do is not None:
+                    main.wait_event(wait_do[c])
+                self._bwd(c, self.chunks[c], start, n, record)
             used[c] = ev()
             used[c].record(main)
             if on_dq is not None:
@@ -416,6 +421,14 @@ class Step:
         if record:
             e1.record()
             self.bwd_events.append((e0, e1, c))
+
+    def _fwd_keep(self, c, ch, start, n):
+        """Chunk c's forward into buffers kept for its backward (no-recompute variant)."""
+        if c not in self.o_keep:
+            self.o_keep[c] = self.torch.empty_like(ch["q"])
+            self.lse_keep[c] = self.torch.empty((self.w.n_q_heads, n), dtype=self.torch.float32, device=self.dev)
+        self.L.oomb_chunk_attn_fwd(self.pool.handle, ch["q"], start, self.sel[c], self.cnt[c], self.scale,
+                                   self.o_keep[c], self.lse_keep[c])
 
     def _fwd(self, c, ch, start, n, record, recompute=False, buf=0):
         L, torch = self.L, self.torch
@@ -1043,16 +1056,19 @@ def main():
     tokens_per_s = job_throughput(w.seq, ms, world)
     rec_ms = sum(a.elapsed_time(b) for a, b, _ in step.recompute_events) / args.steps
     nr_ms = None
-    if not step.offload:  # the variant without recompute, timed directly (forward outputs kept per chunk)
-        step.run(no_recompute=True)
-        torch.cuda.synchronize()
-        n0, n1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # the variant without recompute, timed directly (forward outputs kept per chunk)
+    step.run(no_recompute=True)
+    torch.cuda.synchronize()
+    n0, n1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with gc_paused():
         n0.record()
         for _ in range(args.steps):
             step.run(no_recompute=True)
         n1.record()
         torch.cuda.synchronize()
-        nr_ms = reduce_max_ms(n0.elapsed_time(n1) / args.steps, world, dev)
+    nr_ms = reduce_max_ms(n0.elapsed_time(n1) / args.steps, world, dev)
+    step.o_keep.clear()  # the kept outputs (30 GB at 4M tokens) are not needed again
+    step.lse_keep.clear()
     graph = None if step.offload or args.no_graph else measure_graph(step, args.steps, world, dev)
     kern_ms = sum(a.elapsed_time(b) for ev in (step.fwd_events, step.bwd_events, step.app_events, step.sel_events)
                   for a, b, _ in ev) / args.steps

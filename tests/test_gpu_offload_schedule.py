@@ -5,7 +5,9 @@ against the same workload with every pool in HBM: the same selections, O and LSE
 the forward sweep and the final dK/dV bit for bit, dQ to rounding (its fp32
 reductions across thread blocks run in a run-dependent order), the host K/V pools
 equal to the resident ones; and the same again on a second step (the pools are
-reset and refilled, and state bytes of the gradient blocks restart at empty)."""
+reset and refilled, and state bytes of the gradient blocks restart at empty); and
+the variant that keeps the forward sweep's outputs instead of recomputing them
+gives the same gradients."""
 import dataclasses
 
 import pytest
@@ -57,5 +59,13 @@ def test_offload_schedule_matches_resident(window):
         assert torch.equal(ok.cpu(), rk.cpu()) and torch.equal(ov.cpu(), rv.cpu())
     # the forward of the last chunk (its buffers hold the forward sweep's O and LSE)
     assert torch.equal(off.ob[0], res.ob[0]) and torch.equal(off.lseb[0], res.lseb[0])
+    # without the recomputed forward (outputs kept per chunk): the same gradients bit for bit
+    off.run(no_recompute=True)
+    torch.cuda.synchronize()
+    assert L.oomb_check(off.pool.handle) == 0
+    dk2, dv2 = off.pool.logical_grads(w_off.seq)
+    assert torch.equal(dk2.cpu(), rdk.cpu()) and torch.equal(dv2.cpu(), rdv.cpu())
+    for c in range(w_off.n_chunks):
+        assert O.rel_l2(f64(off.dq[c]), f64(res.dq[c])) < 1e-3, c
     off.pool.close()
     res.pool.close()
