@@ -1214,9 +1214,11 @@ def measure_e2e(step, steps, credited, world, dev):
     chunks from page-locked host memory to the device and reads dQ (and, when the
     gradient pools are in HBM, dK/dV) back, all inside the timed region.  The uploads
     run on a copy stream, chunk by chunk, and each chunk waits only for its own
-    inputs; each dQ is read back on the copy stream as soon as its backward is issued
-    (the pools at the end of the step).  With offloaded gradient pools the step's own
-    write-backs put dK/dV in host memory; those bytes are counted as read back."""
+    inputs; each dQ is read back on the copy stream as soon as its backward is issued,
+    and so are the chunk's dK/dV rows (token-major, gathered through the page table:
+    a chunk's own pages receive nothing from the chunks the reverse sweep has left).
+    With offloaded gradient pools the step's own write-backs put dK/dV in host memory;
+    those bytes are counted as read back."""
     import torch
     sizes = [t.numel() * t.element_size() for ch in step.chunks for t in ch.values()]
     dq_sizes = [d.numel() * d.element_size() for d in step.dq]
@@ -1228,10 +1230,13 @@ def measure_e2e(step, steps, credited, world, dev):
     host_dq = [hb.take(d.shape, d.dtype) for d in step.dq]
     pools_on_device = not step.offload_grads
     host_dk = host_dv = None
-    if pools_on_device:
-        hp = HostBuffer(2 * step.pool.dk_pool.numel() * 4 + 512)
-        host_dk = hp.take(step.pool.dk_pool.shape, torch.float32)
-        host_dv = hp.take(step.pool.dv_pool.shape, torch.float32)
+    w = step.w
+    if pools_on_device:  # token-major dK, dV of the whole sequence; two device gather buffers
+        hp = HostBuffer(2 * w.seq * w.n_kv_heads * w.head_dim * 4 + 512)
+        host_dk = hp.take((w.seq, w.n_kv_heads, w.head_dim), torch.float32)
+        host_dv = hp.take((w.seq, w.n_kv_heads, w.head_dim), torch.float32)
+        gk = [torch.empty((w.chunk, w.n_kv_heads, w.head_dim), dtype=torch.float32, device=dev) for _ in range(2)]
+        gv = [torch.empty_like(gk[0]) for _ in range(2)]
     torch.cuda.synchronize()
     bi = sum(sizes)
     bo = sum(dq_sizes) + (2 * host_dk.numel() * 4 if pools_on_device else 0)
@@ -1281,19 +1286,27 @@ def measure_e2e(step, steps, credited, world, dev):
                 after_main()
                 upload(c - E2E_AHEAD + 1, ["do"], ready_do)
 
+        read = {}
+
         def on_dq(c):
+            if pools_on_device:  # chunk c's dK/dV rows are final: gather them for the copy
+                b = c % 2
+                if b in read:  # the copy of chunk c + 2 out of this buffer has finished
+                    main.wait_event(read[b])
+                start, n = w.chunk_bounds(c)
+                step.L.oomb_grad_gather(step.pool.handle, start, gk[b][:n], gv[b][:n])
             done = torch.cuda.Event()
             done.record(main)
             copy.wait_event(done)
             with torch.cuda.stream(copy):
                 host_dq[c].copy_(step.dq[c], non_blocking=True)
+                if pools_on_device:
+                    host_dk[start:start + n].copy_(gk[b][:n], non_blocking=True)
+                    host_dv[start:start + n].copy_(gv[b][:n], non_blocking=True)
+                    read[b] = torch.cuda.Event()
+                    read[b].record(copy)
 
         step.run(wait_in=ready, on_dq=on_dq, on_fwd=on_fwd, wait_do=ready_do, on_rev=on_rev)
-        if pools_on_device:
-            copy.wait_stream(main)
-            with torch.cuda.stream(copy):
-                host_dk.copy_(step.pool.dk_pool, non_blocking=True)
-                host_dv.copy_(step.pool.dv_pool, non_blocking=True)
         main.wait_stream(copy)
 
     one_step()  # warm-up of the copy path
@@ -1315,8 +1328,8 @@ def measure_e2e(step, steps, credited, world, dev):
             "ms_each_step": [round(x, 2) for x in per_step],
             "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
             "overlap": f"uploads per chunk on a copy stream: Q, K, V {E2E_AHEAD} chunks ahead of the forward "
-                       f"sweep, dO {E2E_AHEAD} chunks ahead of the reverse sweep; dQ read back as each backward "
-                       "is issued"}
+                       f"sweep, dO {E2E_AHEAD} chunks ahead of the reverse sweep; dQ (and dK/dV rows when the "
+                       "pools are in HBM) read back as each backward is issued"}
 
 
 if __name__ == "__main__":
