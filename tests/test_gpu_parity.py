@@ -34,6 +34,12 @@ CASES = {
     # bf16 on a shape the tensor-core kernels do not take (d 64, page 64)
     "bf16_small_d": synth.scaled(QWEN, "bf16_small_d", n_q_heads=6, n_kv_heads=2, head_dim=64, page=64,
                                  seq=1300, chunk=320, top_k=3, plants=2),
+    # tensor-core shape, plain multi-head attention (G = 1): one step per query tile and page
+    "bf16_mha": synth.scaled(QWEN, "bf16_mha", n_q_heads=3, n_kv_heads=3, seq=2900, chunk=640, top_k=5,
+                             plants=2),
+    # tensor-core shape, a wide group (G = 8) over two KV heads
+    "bf16_g8": synth.scaled(QWEN, "bf16_g8", n_q_heads=16, n_kv_heads=2, seq=2500, chunk=768, top_k=4,
+                            plants=2),
 }
 
 
