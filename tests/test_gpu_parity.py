@@ -37,6 +37,9 @@ CASES = {
     # tensor-core shape, plain multi-head attention (G = 1): one step per query tile and page
     "bf16_mha": synth.scaled(QWEN, "bf16_mha", n_q_heads=3, n_kv_heads=3, seq=2900, chunk=640, top_k=5,
                              plants=2),
+    # tensor-core shape, chunks of one page and a last chunk of a single token
+    "bf16_one_page_chunks": synth.scaled(QWEN, "bf16_one_page_chunks", n_q_heads=8, n_kv_heads=2, seq=5 * 128 + 1,
+                                         chunk=128, top_k=2, plants=0),
     # tensor-core shape, a wide group (G = 8) over two KV heads
     "bf16_g8": synth.scaled(QWEN, "bf16_g8", n_q_heads=16, n_kv_heads=2, seq=2500, chunk=768, top_k=4,
                             plants=2),
