@@ -315,20 +315,25 @@ class Step:
             used[c].record(main)
         # reverse sweep (its gathers read every page from the host pools); gradient
         # write-backs go on the write-back stream, beside the gathers
-        ready = {S - 1: prefetch(S - 1, [used[S - 1], wb[S - 1]], prev=None)}
+        # kv_ready[c]: chunk c's K/V (and the gradient blocks from the host) are staged, which
+        # is all its recomputed forward needs; ready[c]: also the blocks carried from chunk
+        # c+1, needed by its backward
+        kv_ready = {S - 1: prefetch(S - 1, [used[S - 1], wb[S - 1]], prev=None)}
+        ready = {S - 1: kv_ready[S - 1]}
         wbg = {}
         for c in range(S - 1, -1, -1):
             if c - 1 >= 0:
                 # buffer (c-1) % 2 was last used by chunk c+1 (its backward and its write-back,
                 # which also wrote host blocks this gather may read), or first by the forward sweep
                 after = ([used[c + 1]] + ([wbg[c + 1]] if c + 1 in wbg else [])) if c + 1 < S else [used[S - 1]]
-                ready[c - 1] = prefetch(c - 1, after, prev=c)
+                kv_ready[c - 1] = ready[c - 1] = prefetch(c - 1, after, prev=c)
             if on_rev is not None:
                 on_rev(c)
-            main.wait_event(ready[c])
+            main.wait_event(kv_ready[c])
             L.oomb_pool_set_stage(h, c % 2)
             start, n = w.chunk_bounds(c)
             if no_recompute:
+                main.wait_event(ready[c])
                 ch = self.chunks[c]
                 L.oomb_chunk_attn_bwd(h, ch["q"], self.o_keep[c], ch["do"], self.lse_keep[c], start, self.sel[c],
                                       self.cnt[c], self.scale, self.dq[c], self.ws_bwd)
@@ -337,6 +342,7 @@ class Step:
                     self._fwd(c, self.chunks[c], start, n, record, recompute=True)
                 if wait_do is not None:
                     main.wait_event(wait_do[c])
+                main.wait_event(ready[c])
                 self._bwd(c, self.chunks[c], start, n, record)
             used[c] = ev()
             used[c].record(main)
