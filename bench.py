@@ -493,7 +493,7 @@ class StackStep:
     width 3584, that the selection does not wait for); the append writes the chunk's
     own pages into their staging slots only, and a second high-priority stream writes
     them to the host pools; in the reverse sweep every layer's K/V and gradient blocks
-    are staged one layer ahead, and the gradient write-backs go on the write-back
+    are staged two layers ahead, and the gradient write-backs go on the write-back
     stream.  One high-priority side stream carries the gathers."""
 
     def __init__(self, w, n_layers, dev, model_dim=3584):
@@ -609,13 +609,17 @@ class StackStep:
 
         side.wait_stream(main)  # the forward sweep's last reads of the staging buffers
         side.wait_stream(side_wb)  # and its write-backs: the reverse sweep gathers every page from the host
-        stage_rev(*ritems[0])
+        # items are staged `ahead` items early: the previous chunk of the staged item's layer
+        # (NL items after it in the reverse order) must have run its backward by then
+        ahead = max(1, min(2, NL - 1))
+        for j in range(min(ahead, len(ritems))):
+            stage_rev(*ritems[j])
         for i, (c, layer) in enumerate(ritems):
             st = self.layers[layer]
             h = st.pool.handle
             start, n = w.chunk_bounds(c)
-            if i + 1 < len(ritems):
-                c2, l2 = ritems[i + 1]
+            if i + ahead < len(ritems):
+                c2, l2 = ritems[i + ahead]
                 if c2 + 1 < S and (c2 + 1, l2) not in bwd_done:
                     raise RuntimeError("stack order: the previous chunk of a layer must have run its backward")
                 stage_rev(c2, l2)
