@@ -586,7 +586,7 @@ class StackStep:
             L.oomb_pool_set_stage(h, c % 2)
             self._main(record, L.oomb_chunk_attn_fwd, h, st.chunks[c]["q"], start, st.sel[c], st.cnt[c], st.scale,
                        st.ob[0][:n], st.lseb[0] if n == w.chunk else st.lse_tail(n))
-        # reverse sweep: every item's K/V and gradient blocks staged one item ahead
+        # reverse sweep: every item's K/V and gradient blocks staged ahead of it
         ritems = items[::-1]
         bwd_done, ready, wbg = {}, {}, {}
 

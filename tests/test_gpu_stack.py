@@ -1,6 +1,6 @@
 """The multi-layer offload step (bench.StackStep): layers run chunk by chunk in model
 order, local layers' pages staged one layer ahead, top-K layers' history pages moved
-while a K/V projection GEMM runs, reverse-sweep blocks staged one layer ahead.  The
+while a K/V projection GEMM runs, reverse-sweep blocks staged two layers ahead.  The
 schedule must not change any result: every layer's selections, dQ and final
 gradient pools equal those of the same layer run alone through the single-layer
 offload step (selections and dK/dV bit for bit, dQ to rounding: its fp32 reductions
