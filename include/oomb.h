@@ -170,7 +170,7 @@ OOMB_API oomb_status oomb_kv_append_deferred(oomb_pool* pool, const void* k, con
 /* The reverse of oomb_prefetch_pages: every selected block of a page in
  * [first_page, end_page) is copied from staging buffer stage_buf to its block of
  * the host K/V pools.  Used after oomb_kv_append_deferred with the chunk's own pages
- * as the range.  Errors: ARG, UNSUPPORTED (not an offload pool), CUDA. */
+ * as the range.  Errors: ARG, ALIGN, UNSUPPORTED (not an offload pool), CUDA. */
 OOMB_API oomb_status oomb_kv_writeback(oomb_pool* pool, const int32_t* sel, const int32_t* sel_count, int max_sel,
                                        int stage_buf, int64_t first_page, int64_t end_page, void* stream);
 
@@ -317,8 +317,8 @@ OOMB_API oomb_status oomb_chunk_attn_bwd(oomb_pool* pool, const void* q, const v
  * selected (page, KV head) blocks of K and V from the pinned host pools into
  * staging buffer `stage_buf` (0 or 1) on `stream` (normally a side stream;
  * order it against the attention calls with CUDA events).  Block s of KV head h
- * lands in slot (stage_buf, h, s).  Errors: ARG, UNSUPPORTED (pool not in
- * offload mode), CUDA. */
+ * lands in slot (stage_buf, h, s).  Errors: ARG, ALIGN (selection not 4-byte
+ * aligned), UNSUPPORTED (pool not in offload mode), CUDA. */
 OOMB_API oomb_status oomb_prefetch(oomb_pool* pool, const int32_t* sel, const int32_t* sel_count, int max_sel,
                           int stage_buf, void* stream);
 

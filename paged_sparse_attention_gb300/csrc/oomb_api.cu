@@ -436,6 +436,7 @@ oomb_status oomb_prefetch_pages(oomb_pool* p, const int32_t* sel, const int32_t*
   if (!p || !sel || !sel_count || max_sel <= 0 || first_page < 0 || end_page < first_page) return OOMB_ERR_ARG;
   if (!p->d.offload) return OOMB_ERR_UNSUPPORTED;
   if (stage_buf < 0 || stage_buf > 1 || max_sel > p->d.stage_max_sel) return OOMB_ERR_ARG;
+  if (!aligned(sel, 4) || !aligned(sel_count, 4)) return OOMB_ERR_ALIGN;
   const int lo = (int)std::min<int64_t>(first_page, INT32_MAX), hi = (int)std::min<int64_t>(end_page, INT32_MAX);
   return cuda_status(launch_prefetch(p->g, p->d.k_pool, p->d.v_pool, p->d.page_table, sel, sel_count, max_sel,
                                      p->d.stage_k, p->d.stage_v, stage_buf * p->g.Hkv, p->d.stage_max_sel, lo, hi,
@@ -447,6 +448,7 @@ oomb_status oomb_kv_writeback(oomb_pool* p, const int32_t* sel, const int32_t* s
   if (!p || !sel || !sel_count || max_sel <= 0 || first_page < 0 || end_page < first_page) return OOMB_ERR_ARG;
   if (!p->d.offload) return OOMB_ERR_UNSUPPORTED;
   if (stage_buf < 0 || stage_buf > 1 || max_sel > p->d.stage_max_sel) return OOMB_ERR_ARG;
+  if (!aligned(sel, 4) || !aligned(sel_count, 4)) return OOMB_ERR_ALIGN;
   const int lo = (int)std::min<int64_t>(first_page, INT32_MAX), hi = (int)std::min<int64_t>(end_page, INT32_MAX);
   return cuda_status(launch_prefetch(p->g, p->d.k_pool, p->d.v_pool, p->d.page_table, sel, sel_count, max_sel,
                                      p->d.stage_k, p->d.stage_v, stage_buf * p->g.Hkv, p->d.stage_max_sel, lo, hi,

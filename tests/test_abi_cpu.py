@@ -70,6 +70,8 @@ def test_offload_pool_host_checks(lib):
     assert lib.oomb_kv_writeback(pool, fake, fake, 8, 2, 0, 1, None) == 1
     assert lib.oomb_kv_writeback(pool, fake, fake, 9, 0, 0, 1, None) == 1
     assert lib.oomb_prefetch_pages(pool, fake, fake, 8, 0, 3, 2, None) == 1
+    assert lib.oomb_prefetch(pool, fake + 2, fake, 8, 0, None) == 3  # misaligned selection
+    assert lib.oomb_kv_writeback(pool, fake, fake + 1, 8, 0, 0, 1, None) == 3
     assert lib.oomb_pool_free_pages(pool) == 4  # nothing was taken
     lib.oomb_pool_destroy(pool)
 
