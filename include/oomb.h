@@ -228,6 +228,31 @@ OOMB_API oomb_status oomb_page_select(oomb_pool* pool, const void* q, int64_t q_
                              int32_t* sel, int32_t* sel_count, int max_sel, void* workspace, size_t ws_bytes,
                              void* stream);
 
+/* Where oomb_page_select_append writes the chunk's pages. */
+typedef enum {
+  OOMB_APPEND_POOL = 0,     /* the pools, as oomb_kv_append */
+  OOMB_APPEND_STAGED = 1,   /* the pools and the staging slots, as oomb_kv_append_staged */
+  OOMB_APPEND_DEFERRED = 2  /* the staging slots only, as oomb_kv_append_deferred */
+} oomb_append_mode;
+
+/* The selection of one chunk and the append of that chunk's own K/V in one launch
+ * (explainer 2.D: pages are selected by their summaries; 2.B: the chunk's K/V go to
+ * free pages).  Same results as oomb_page_select followed by the append named by
+ * append_mode with k, v ([n_q, Hkv, d], first token q_start): the selection reads
+ * only history pages and the append writes only the chunk's own pages, so when the
+ * selection scores pages (more mapped candidates than top_k > 0) the selection's grid
+ * also appends, before its query sum, with the append kernel's arithmetic (bit-
+ * identical pools, summaries and slots); otherwise the two run as two launches.  The
+ * own pages' staging slots need no selection result: the count of a top-K selection
+ * is known beforehand (mapped sinks + min(top_k, mapped candidates) + own pages).
+ * q_start must equal the tokens appended so far.  stage_buf: the staging buffer for
+ * the STAGED and DEFERRED modes (offload pools only).  Errors: those of both calls;
+ * nothing is appended when an error is returned. */
+OOMB_API oomb_status oomb_page_select_append(oomb_pool* pool, const void* q, const void* k, const void* v,
+                                            int64_t q_start, int n_q, int top_k, int n_sink, int32_t* sel,
+                                            int32_t* sel_count, int max_sel, void* workspace, size_t ws_bytes,
+                                            int append_mode, int stage_buf, void* stream);
+
 /* oomb_page_select for callers that cannot allocate device memory.  The pages
  * describe no counterpart: this is a property of the library, not of the method.
  * Identical selection to oomb_page_select, but the scratch it needs comes from a

@@ -65,6 +65,7 @@ def load(path: str = LIB_PATH) -> C.CDLL:
         "oomb_kv_append": (i32, [vp, vp, vp, i64, i32, vp]),
         "oomb_kv_append_staged": (i32, [vp, vp, vp, i64, i32, vp, i32, i32, vp]),
         "oomb_kv_append_deferred": (i32, [vp, vp, vp, i64, i32, vp, i32, i32, vp]),
+        "oomb_page_select_append": (i32, [vp, vp, vp, vp, i64, i32, i32, i32, vp, vp, i32, vp, sz, i32, i32, vp]),
         "oomb_kv_writeback": (i32, [vp, vp, vp, i32, i32, i64, i64, vp]),
         "oomb_page_select": (i32, [vp, vp, i64, i32, i32, i32, vp, vp, i32, vp, sz, vp]),
         "oomb_chunk_attn_fwd": (i32, [vp, vp, i64, i32, vp, vp, i32, f32, vp, vp, vp]),
@@ -292,6 +293,21 @@ def oomb_uses_tensor_cores(pool: int) -> bool:
 
 def oomb_launch_count() -> int:
     return int(load().oomb_launch_count())
+
+
+OOMB_APPEND_POOL, OOMB_APPEND_STAGED, OOMB_APPEND_DEFERRED = 0, 1, 2
+
+
+def oomb_page_select_append(pool: int, q, k, v, q_start: int, top_k: int, n_sink: int, sel, sel_count, workspace,
+                            append_mode: int = OOMB_APPEND_POOL, stage_buf: int = 0, n_q: Optional[int] = None,
+                            stream=None) -> None:
+    """oomb_page_select and the append of the chunk's K/V (the chunk's tokens) in one call."""
+    n = q.shape[0] if n_q is None else n_q
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _ok("oomb_page_select_append", load().oomb_page_select_append(pool, _ptr(q), _ptr(k), _ptr(v), q_start, n, top_k,
+                                                                  n_sink, _ptr(sel), _ptr(sel_count), sel.shape[-1],
+                                                                  _ptr(workspace), ws_bytes, append_mode, stage_buf,
+                                                                  _stream(stream)))
 
 
 def oomb_page_select_noalloc(pool: int, q, q_start: int, top_k: int, n_sink: int, sel, sel_count,

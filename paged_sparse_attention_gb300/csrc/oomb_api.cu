@@ -5,6 +5,7 @@
 #include <cstring>
 #include <new>
 
+#include "append_unit.cuh"
 #include "oomb_internal.h"
 
 using namespace oomb;
@@ -218,9 +219,22 @@ uint64_t oomb_launch_count(void) { return g_launches.load(std::memory_order_rela
 
 int oomb_uses_tensor_cores(const oomb_pool* p) { return p && tc_supported(p->g) ? 1 : 0; }
 
-// Shared body of oomb_kv_append and oomb_kv_append_staged.
-static oomb_status kv_append_impl(oomb_pool* p, const void* k, const void* v, int64_t first_token, int n_tokens,
-                                  const StageArgs* stage, void* stream) {
+// An append about to be launched: its new pages are taken from the free list and
+// entered in the host table; undone by release() if the launch fails.
+struct PendingAppend {
+  std::vector<int32_t> newp;
+  int64_t first_page = 0, end = 0;
+  int n_new = 0;
+  void release(oomb_pool* p) {
+    for (int i = n_new - 1; i >= 0; --i) {
+      p->free_list.push_back(newp[i]);
+      p->table[first_page + i] = -1;
+    }
+  }
+};
+
+static oomb_status prepare_append(oomb_pool* p, const void* k, const void* v, int64_t first_token, int n_tokens,
+                                  void* stream, PendingAppend* pa) {
   if (!p || !k || !v || n_tokens <= 0 || first_token < 0) return OOMB_ERR_ARG;
   if (first_token != p->n_tokens) return OOMB_ERR_ARG;
   if (first_token % p->g.P != 0) return OOMB_ERR_ALIGN;
@@ -234,24 +248,33 @@ static oomb_status kv_append_impl(oomb_pool* p, const void* k, const void* v, in
   if (n_new > (int)p->free_list.size()) return OOMB_ERR_OUT_OF_PAGES;
   cudaError_t e = clear_table_if_dirty(p, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_status(e);
-  std::vector<int32_t> newp(n_new);
+  pa->newp.resize(n_new);
   for (int i = 0; i < n_new; ++i) {
-    newp[i] = p->free_list.back();
+    pa->newp[i] = p->free_list.back();
     p->free_list.pop_back();
-    p->table[first_page + i] = newp[i];
+    p->table[first_page + i] = pa->newp[i];
   }
-  e = launch_kv_append(p->g, p->d.k_pool, p->d.v_pool, p->d.dk_pool, p->d.dv_pool, p->d.summary,
-                                   p->d.page_table, k, v, first_token, n_tokens, end, newp.data(), n_new,
-                                   (int)first_page, p->d.offload_grads ? p->d.grad_state : nullptr, stage,
+  pa->first_page = first_page;
+  pa->end = end;
+  pa->n_new = n_new;
+  return OOMB_OK;
+}
+
+// Shared body of oomb_kv_append, oomb_kv_append_staged and oomb_kv_append_deferred.
+static oomb_status kv_append_impl(oomb_pool* p, const void* k, const void* v, int64_t first_token, int n_tokens,
+                                  const StageArgs* stage, void* stream) {
+  PendingAppend pa;
+  oomb_status s = prepare_append(p, k, v, first_token, n_tokens, stream, &pa);
+  if (s != OOMB_OK) return s;
+  cudaError_t e = launch_kv_append(p->g, p->d.k_pool, p->d.v_pool, p->d.dk_pool, p->d.dv_pool, p->d.summary,
+                                   p->d.page_table, k, v, first_token, n_tokens, pa.end, pa.newp.data(), pa.n_new,
+                                   (int)pa.first_page, p->d.offload_grads ? p->d.grad_state : nullptr, stage,
                                    p->d.error_word, (cudaStream_t)stream);
   if (e != cudaSuccess) {
-    for (int i = n_new - 1; i >= 0; --i) {
-      p->free_list.push_back(newp[i]);
-      p->table[first_page + i] = -1;
-    }
+    pa.release(p);
     return cuda_status(e);
   }
-  p->n_tokens = end;
+  p->n_tokens = pa.end;
   return OOMB_OK;
 }
 
@@ -320,9 +343,17 @@ size_t oomb_workspace_size(const oomb_pool* p, int op, int n_q) {
   return 0;
 }
 
-oomb_status oomb_page_select(oomb_pool* p, const void* q, int64_t q_start, int n_q, int top_k, int n_sink,
-                             int32_t* sel, int32_t* sel_count, int max_sel, void* ws, size_t ws_bytes,
-                             void* stream) {
+// What a top-K selection of one chunk will hold, known on the host: the mapped
+// candidates, whether any sink or candidate is freed, and the entry count per KV head
+// (the same for every head: mapped sinks + kept candidates + own pages).
+struct SelectPlan {
+  int64_t mapped = 0, count = 0, n_own = 0;
+  int any_unmapped = 0;
+};
+
+static oomb_status plan_select(oomb_pool* p, const void* q, int64_t q_start, int n_q, int top_k, int n_sink,
+                               int32_t* sel, int32_t* sel_count, int max_sel, void* ws, size_t ws_bytes,
+                               SelectPlan* plan) {
   oomb_status s = check_chunk(p, q, q_start, n_q, sel, sel_count, max_sel, false);
   if (s != OOMB_OK) return s;
   if (top_k < -1 || n_sink < 0) return OOMB_ERR_ARG;
@@ -343,9 +374,78 @@ oomb_status oomb_page_select(oomb_pool* p, const void* q, int64_t q_start, int n
   size_t need = select_workspace_bytes(p->g, n_q);
   if (!ws || ws_bytes < need) return OOMB_ERR_WORKSPACE;
   if (!aligned(ws, 16)) return OOMB_ERR_ALIGN;
+  plan->mapped = mapped;
+  plan->count = sinks - freed_sinks + kept + n_own;
+  plan->n_own = n_own;
+  plan->any_unmapped = (freed_sinks + freed_cand) > 0 ? 1 : 0;
+  return OOMB_OK;
+}
+
+oomb_status oomb_page_select(oomb_pool* p, const void* q, int64_t q_start, int n_q, int top_k, int n_sink,
+                             int32_t* sel, int32_t* sel_count, int max_sel, void* ws, size_t ws_bytes,
+                             void* stream) {
+  SelectPlan plan;
+  oomb_status s = plan_select(p, q, q_start, n_q, top_k, n_sink, sel, sel_count, max_sel, ws, ws_bytes, &plan);
+  if (s != OOMB_OK) return s;
   return cuda_status(launch_page_select(p->g, p->d.summary, p->d.page_table, q, q_start, n_q, top_k, n_sink,
-                                        (int)mapped, (freed_sinks + freed_cand) > 0 ? 1 : 0, sel, sel_count, max_sel,
-                                        ws, p->d.error_word, p->d.error_word, (cudaStream_t)stream));
+                                        (int)plan.mapped, plan.any_unmapped, sel, sel_count, max_sel, ws,
+                                        p->d.error_word, p->d.error_word, (cudaStream_t)stream));
+}
+
+oomb_status oomb_page_select_append(oomb_pool* p, const void* q, const void* k, const void* v, int64_t q_start,
+                                    int n_q, int top_k, int n_sink, int32_t* sel, int32_t* sel_count, int max_sel,
+                                    void* ws, size_t ws_bytes, int append_mode, int stage_buf, void* stream) {
+  if (!p) return OOMB_ERR_ARG;
+  if (append_mode < OOMB_APPEND_POOL || append_mode > OOMB_APPEND_DEFERRED) return OOMB_ERR_ARG;
+  if (append_mode != OOMB_APPEND_POOL) {
+    if (!p->d.offload) return OOMB_ERR_UNSUPPORTED;
+    if (stage_buf < 0 || stage_buf > 1 || max_sel > p->d.stage_max_sel) return OOMB_ERR_ARG;
+  }
+  if (q_start != p->n_tokens) return OOMB_ERR_ARG;  // the chunk's K/V are appended now
+  SelectPlan plan;
+  oomb_status s = plan_select(p, q, q_start, n_q, top_k, n_sink, sel, sel_count, max_sel, ws, ws_bytes, &plan);
+  if (s != OOMB_OK) return s;
+  PendingAppend pa;
+  s = prepare_append(p, k, v, q_start, n_q, stream, &pa);
+  if (s != OOMB_OK) return s;
+  StageArgs sa;
+  const StageArgs* stage = nullptr;
+  if (append_mode != OOMB_APPEND_POOL) {
+    sa.k = p->d.stage_k;
+    sa.v = p->d.stage_v;
+    sa.sel_count = sel_count;
+    sa.stage_h0 = stage_buf * p->g.Hkv;
+    sa.stride = p->d.stage_max_sel;
+    sa.max_sel = max_sel;
+    sa.skip_pool = append_mode == OOMB_APPEND_DEFERRED ? 1 : 0;
+    sa.slot0 = (int)(plan.count - plan.n_own);  // own page 0's entry, the same for every KV head
+    stage = &sa;
+  }
+  uint8_t* gs = p->d.offload_grads ? p->d.grad_state : nullptr;
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaError_t e;
+  if (select_scores(q_start, n_sink, top_k, (int)plan.mapped, p->g) && pa.n_new <= kMaxFusedAppendPages) {
+    // one launch: the selection's grid appends the chunk's pages before its query sum
+    const AppendJob job = append_job(p->g, p->d.k_pool, p->d.v_pool, p->d.dk_pool, p->d.dv_pool, p->d.summary,
+                                     p->d.page_table, k, v, q_start, pa.end, pa.n_new, (int)pa.first_page, gs,
+                                     stage, p->d.error_word);
+    e = launch_page_select(p->g, p->d.summary, p->d.page_table, q, q_start, n_q, top_k, n_sink, (int)plan.mapped,
+                           plan.any_unmapped, sel, sel_count, max_sel, ws, p->d.error_word, p->d.error_word, st,
+                           &job, pa.newp.data(), pa.n_new);
+  } else {  // a selection that scores nothing (or a very long chunk): two launches
+    e = launch_page_select(p->g, p->d.summary, p->d.page_table, q, q_start, n_q, top_k, n_sink, (int)plan.mapped,
+                           plan.any_unmapped, sel, sel_count, max_sel, ws, p->d.error_word, p->d.error_word, st);
+    if (e == cudaSuccess)
+      e = launch_kv_append(p->g, p->d.k_pool, p->d.v_pool, p->d.dk_pool, p->d.dv_pool, p->d.summary,
+                           p->d.page_table, k, v, q_start, n_q, pa.end, pa.newp.data(), pa.n_new, (int)pa.first_page,
+                           gs, stage, p->d.error_word, st);
+  }
+  if (e != cudaSuccess) {
+    pa.release(p);
+    return cuda_status(e);
+  }
+  p->n_tokens = pa.end;
+  return OOMB_OK;
 }
 
 oomb_status oomb_window_select(oomb_pool* p, int64_t q_start, int n_q, int window, int n_sink, int32_t* sel,

@@ -61,6 +61,7 @@ struct StageArgs {
   const int32_t* sel_count;
   int stage_h0, stride, max_sel;
   int skip_pool;  // 1: the new pages go to the staging slots only (the host pools later)
+  int slot0 = -1; // >= 0: staging slot of own page 0 for every KV head (else read from sel_count)
 };
 
 // ---- launchers (return cudaGetLastError of the launch) ----
@@ -73,10 +74,17 @@ cudaError_t launch_kv_append(const Geometry& g, void* k_pool, void* v_pool, floa
 size_t select_workspace_bytes(const Geometry& g, int n_q);
 // n_mapped_cand: candidate pages [n_sink', q_start/P) whose table entry is mapped;
 // any_unmapped: some sink or candidate page is unmapped (freed) and must be skipped.
+// job/new_phys/n_new: an append fused into the launch (only where select_scores holds and
+// n_new <= kMaxFusedAppendPages; the append's staging slot must then be known, slot0 >= 0).
+struct AppendJob;
+constexpr int kMaxFusedAppendPages = 256;
 cudaError_t launch_page_select(const Geometry& g, const float* summary, const int32_t* table, const void* q,
                                int64_t q_start, int n_q, int top_k, int n_sink, int n_mapped_cand, int any_unmapped,
                                int32_t* sel, int32_t* sel_count, int max_sel, void* ws, uint32_t* err, uint32_t* ctrl,
-                               cudaStream_t st);
+                               cudaStream_t st, const AppendJob* job = nullptr, const int32_t* new_phys = nullptr,
+                               int n_new = 0);
+// The selection scores pages (the cooperative grid runs), given the mapped candidates.
+bool select_scores(int64_t q_start, int n_sink, int top_k, int n_mapped_cand, const Geometry& g);
 
 // sel[h] = [0, sinks) U [lo, own_end) for every KV head h (host-validated bounds)
 cudaError_t launch_window_select(const Geometry& g, int sinks, int lo, int own_end, int32_t* sel,

@@ -23,6 +23,10 @@
 //   3. page scores   qbar[h] . summary row, from shared memory; each score is
 //                    stored as an order-preserving 32-bit key and counted in a
 //                    per-head histogram of its top 12 bits (global atomics)
+//   (with an append fused in: before phase 1, the CTA's two 256-thread halves append
+//    (new page, KV head) units of the chunk's own K/V, append_unit.cuh, the same
+//    arithmetic as the append kernel; the selection reads only history pages, the
+//    append writes only the own pages, so the two share nothing)
 //   4. top-k         one CTA per KV head: the histogram gives the 12-bit prefix of
 //                    the k-th largest key; the keys in that bin are gathered and a
 //                    bitwise search over the remaining 20 bits finds the exact
@@ -31,6 +35,7 @@
 // Every sum runs in a fixed order and the histogram is integer, so the selection
 // is deterministic.  The barrier counters live in the pool's control block and
 // are sense-reversing (see grid_sync): the host keeps no state between calls.
+#include "append_unit.cuh"
 #include "oomb_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -78,6 +83,10 @@ struct SelParams {
   int32_t* sel_count;
   uint32_t* err;
   uint32_t* ctrl;
+  // the fused append (n_new > 0): the chunk's own pages, new_phys[i] for own page i
+  int n_new;
+  AppendJob job;
+  int32_t new_phys[kMaxFusedAppendPages];
 };
 
 
@@ -664,7 +673,7 @@ __device__ void top_k_head(const SelParams& p, int h, uint32_t* sh_keys) {
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kThreads, 1) page_select_kernel(const SelParams p) {
+__global__ void __launch_bounds__(kThreads, 1) page_select_kernel(const __grid_constant__ SelParams p) {
   extern __shared__ __align__(128) float sh[];
   __shared__ uint64_t sum_full[2];
   __shared__ int abort_flag;
@@ -690,6 +699,17 @@ __global__ void __launch_bounds__(kThreads, 1) page_select_kernel(const SelParam
     const int hn = p.g.Hkv * kHistBins, hs = (hn + gridDim.x - 1) / gridDim.x;
     const int h0 = blockIdx.x * hs, h1 = min(hn, h0 + hs);
     for (int i = h0 + threadIdx.x; i < h1; i += kThreads) p.hist[i] = 0u;
+    if (p.n_new > 0) {
+      // the fused append: unit u = (own page u / Hkv, KV head u % Hkv), two at a time per
+      // CTA, each half of the CTA on its own named barrier; `sh` is free until phase 1
+      const int half = threadIdx.x / kAppendThreads;
+      float* part = sh + half * kAppendThreads * 8;
+      const int units = p.n_new * p.g.Hkv;
+      for (int u = 2 * blockIdx.x + half; u < units; u += 2 * gridDim.x)
+        append_unit<T, 2>(p.job, p.new_phys[u / p.g.Hkv], u / p.g.Hkv, u % p.g.Hkv, threadIdx.x % kAppendThreads,
+                          part, 1 + half);
+      __syncthreads();
+    }
     query_sum<T>(p, sh);
     if (!grid_sync(p, 0, true)) return;
     mean_query(p, sh);
@@ -709,6 +729,12 @@ size_t query_sum_smem(const Geometry& g) {
 
 }  // namespace
 
+bool select_scores(int64_t q_start, int n_sink, int top_k, int n_mapped_cand, const Geometry& g) {
+  const int n_hist = (int)(q_start / g.P);
+  const int n_cand = n_hist - (n_sink < n_hist ? n_sink : n_hist);
+  return n_cand > 0 && top_k > 0 && n_mapped_cand > top_k;
+}
+
 size_t select_workspace_bytes(const Geometry& g, int n_q) {
   (void)n_q;
   const size_t HD = (size_t)g.Hkv * g.d;
@@ -718,10 +744,17 @@ size_t select_workspace_bytes(const Geometry& g, int n_q) {
 cudaError_t launch_page_select(const Geometry& g, const float* summary, const int32_t* table, const void* q,
                                int64_t q_start, int n_q, int top_k, int n_sink, int n_mapped_cand, int any_unmapped,
                                int32_t* sel, int32_t* sel_count, int max_sel, void* ws, uint32_t* err, uint32_t* ctrl,
-                               cudaStream_t st) {
+                               cudaStream_t st, const AppendJob* job, const int32_t* new_phys, int n_new) {
   const size_t HD = (size_t)g.Hkv * g.d;
   char* w = (char*)ws;
   SelParams p;
+  p.n_new = 0;
+  if (job) {  // the caller has checked fused_append_ok
+    if (n_new <= 0 || n_new > kMaxFusedAppendPages) return cudaErrorInvalidValue;
+    p.n_new = n_new;
+    p.job = *job;
+    for (int i = 0; i < n_new; ++i) p.new_phys[i] = new_phys[i];
+  }
   p.g = g;
   p.q = q;
   p.n_q = n_q;
@@ -759,6 +792,7 @@ cudaError_t launch_page_select(const Geometry& g, const float* summary, const in
   const bool bf16 = g.dtype != OOMB_FP32;
   const void* fn = bf16 ? (const void*)page_select_kernel<__nv_bfloat16> : (const void*)page_select_kernel<float>;
   if (!p.need_scores) {
+    if (job) return cudaErrorInvalidValue;  // a fused append needs the cooperative grid
     void* args[] = {&p};
     cudaError_t e = cudaLaunchKernel(fn, dim3(g.Hkv), dim3(kThreads), args, 0, st);
     count_launches(1);
@@ -775,7 +809,8 @@ cudaError_t launch_page_select(const Geometry& g, const float* summary, const in
                                                             kSumBytesCap / 2 / row_bytes));
   const int n4 = (int)(HD / 4), groups = std::max(1, kThreads / n4);
   const size_t qbar_bytes = HD * sizeof(float) + (size_t)groups * std::min(n4, kThreads) * 16;
-  const size_t front = align_up(std::max(query_sum_smem(g), qbar_bytes), 128);
+  size_t front = align_up(std::max(query_sum_smem(g), qbar_bytes), 128);
+  if (job) front = std::max(front, (size_t)2 * kAppendThreads * 8 * sizeof(float));  // the append halves' `part`
   p.sum_off = (uint32_t)front;
   size_t smem = front + 2 * (size_t)p.half_pages * row_bytes;
   if (p.keys_in_smem) smem = std::max(smem, align_up((size_t)p.n_cand, 4) * sizeof(uint32_t));

@@ -563,3 +563,71 @@ def test_select_skips_freed_pages():
                 L.oomb_page_select(pool.handle, q, start, -1, 2, sel, cnt, ws)
     assert L.oomb_check(pool.handle) == 0
     pool.close()
+
+
+@pytest.mark.parametrize("mode", ["pool", "staged", "deferred"])
+def test_select_append_fused_matches_separate(mode):
+    """oomb_page_select_append against oomb_page_select followed by the append of the
+    same mode, chunk by chunk over a sweep whose early chunks keep every candidate (two
+    launches) and whose later chunks score pages (one launch): the same selections,
+    page table, K/V pools, summaries, zeroed gradient pages and staging slots, bit for
+    bit.  The staged modes run on offload pools with the gradients in host memory."""
+    w = synth.scaled(QWEN, f"fused_{mode}", seq=11 * 512 + 200, chunk=512, top_k=3, plants=2)
+    chunks, _ = make_chunks(w)
+    order = synth.page_order(w)
+    dev = torch.device("cuda")
+    off = mode != "pool"
+
+    def new_pool():
+        return PagedKVPool(w.n_q_heads, w.n_kv_heads, w.head_dim, w.page, w.num_phys, w.n_pages, w.torch_dtype,
+                           dev, page_order=order, offload=off, stage_max_sel=w.max_sel if off else 0,
+                           offload_grads=off)
+
+    sep, fus = new_pool(), new_pool()
+    if off:  # slots the appends do not write must compare equal too
+        for pl in (sep, fus):
+            pl.stage_k.zero_()
+            pl.stage_v.zero_()
+    ws_s, ws_f = sep.workspace(L.OOMB_OP_SELECT, w.chunk), fus.workspace(L.OOMB_OP_SELECT, w.chunk)
+    am = {"pool": L.OOMB_APPEND_POOL, "staged": L.OOMB_APPEND_STAGED, "deferred": L.OOMB_APPEND_DEFERRED}[mode]
+    scored = 0
+    for c, ch in enumerate(chunks):
+        start, n = w.chunk_bounds(c)
+        q, k, v = (ch[x].to(dev) for x in ("q", "k", "v"))
+        outs = []
+        for pl, ws, fused in ((sep, ws_s, False), (fus, ws_f, True)):
+            sel = torch.full((w.n_kv_heads, w.max_sel), -1, dtype=torch.int32, device=dev)
+            cnt = torch.zeros(w.n_kv_heads, dtype=torch.int32, device=dev)
+            if fused:
+                L.oomb_page_select_append(pl.handle, q, k, v, start, w.top_k, w.n_sink, sel, cnt, ws, am, c % 2)
+            else:
+                L.oomb_page_select(pl.handle, q, start, w.top_k, w.n_sink, sel, cnt, ws)
+                if mode == "pool":
+                    L.oomb_kv_append(pl.handle, k, v, start)
+                elif mode == "staged":
+                    L.oomb_kv_append_staged(pl.handle, k, v, start, cnt, w.max_sel, c % 2)
+                else:
+                    L.oomb_kv_append_deferred(pl.handle, k, v, start, cnt, w.max_sel, c % 2)
+            outs.append((sel, cnt))
+        torch.cuda.synchronize()
+        assert torch.equal(outs[0][1], outs[1][1]) and torch.equal(outs[0][0], outs[1][0]), c
+        n_hist = start // w.page
+        scored += int(max(0, n_hist - w.n_sink) > w.top_k)
+        if off:  # this chunk's staging buffer (its own slots were written by the append)
+            assert torch.equal(sep.stage_k[c % 2], fus.stage_k[c % 2]) and torch.equal(sep.stage_v[c % 2],
+                                                                                          fus.stage_v[c % 2]), c
+    assert scored >= 5  # the fused single launch was exercised
+    assert L.oomb_check(sep.handle) == 0 and L.oomb_check(fus.handle) == 0
+    assert sep.table_host(w.n_pages) == fus.table_host(w.n_pages)
+    assert torch.equal(sep.summary, fus.summary)
+    if mode != "deferred":
+        ks, vs = sep.logical_kv(w.seq)
+        kf, vf = fus.logical_kv(w.seq)
+        assert torch.equal(ks, kf) and torch.equal(vs, vf)
+        assert torch.equal(ks.cpu(), torch.cat([ch["k"] for ch in chunks]))
+    if off:
+        assert torch.equal(sep.grad_state, fus.grad_state)
+    else:
+        assert torch.equal(sep.dk_pool, fus.dk_pool) and torch.equal(sep.dv_pool, fus.dv_pool)
+    sep.close()
+    fus.close()
