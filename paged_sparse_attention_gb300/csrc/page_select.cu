@@ -83,7 +83,10 @@ struct SelParams {
   int32_t* sel_count;
   uint32_t* err;
   uint32_t* ctrl;
-  // the fused append (n_new > 0): the chunk's own pages, new_phys[i] for own page i
+};
+
+// The append fused into a selection: the chunk's own pages, new_phys[i] for own page i.
+struct FusedAppend {
   int n_new;
   AppendJob job;
   int32_t new_phys[kMaxFusedAppendPages];
@@ -672,8 +675,9 @@ __device__ void top_k_head(const SelParams& p, int h, uint32_t* sh_keys) {
   __syncthreads();  // shared memory is reused by the next head
 }
 
-template <typename T>
-__global__ void __launch_bounds__(kThreads, 1) page_select_kernel(const __grid_constant__ SelParams p) {
+// The selection, with (FUSED) or without the chunk's append before its query sum.
+template <typename T, bool FUSED>
+__device__ __forceinline__ void select_main(const SelParams& p, const FusedAppend* fa) {
   extern __shared__ __align__(128) float sh[];
   __shared__ uint64_t sum_full[2];
   __shared__ int abort_flag;
@@ -699,15 +703,15 @@ __global__ void __launch_bounds__(kThreads, 1) page_select_kernel(const __grid_c
     const int hn = p.g.Hkv * kHistBins, hs = (hn + gridDim.x - 1) / gridDim.x;
     const int h0 = blockIdx.x * hs, h1 = min(hn, h0 + hs);
     for (int i = h0 + threadIdx.x; i < h1; i += kThreads) p.hist[i] = 0u;
-    if (p.n_new > 0) {
+    if (FUSED) {
       // the fused append: unit u = (own page u / Hkv, KV head u % Hkv), two at a time per
       // CTA, each half of the CTA on its own named barrier; `sh` is free until phase 1
       const int half = threadIdx.x / kAppendThreads;
       float* part = sh + half * kAppendThreads * 8;
-      const int units = p.n_new * p.g.Hkv;
+      const int units = fa->n_new * p.g.Hkv;
       for (int u = 2 * blockIdx.x + half; u < units; u += 2 * gridDim.x)
-        append_unit<T, 2>(p.job, p.new_phys[u / p.g.Hkv], u / p.g.Hkv, u % p.g.Hkv, threadIdx.x % kAppendThreads,
-                          part, 1 + half);
+        append_unit<T, 2>(fa->job, fa->new_phys[u / p.g.Hkv], u / p.g.Hkv, u % p.g.Hkv,
+                          threadIdx.x % kAppendThreads, part, 1 + half);
       __syncthreads();
     }
     query_sum<T>(p, sh);
@@ -718,6 +722,17 @@ __global__ void __launch_bounds__(kThreads, 1) page_select_kernel(const __grid_c
     if (!grid_sync(p, 1, selects) || !selects || !ok) return;
   }
   for (int h = blockIdx.x; h < p.g.Hkv; h += gridDim.x) top_k_head(p, h, reinterpret_cast<uint32_t*>(sh));
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 1) page_select_kernel(const SelParams p) {
+  select_main<T, false>(p, nullptr);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 1)
+    page_select_append_kernel(const SelParams p, const __grid_constant__ FusedAppend fa) {
+  select_main<T, true>(p, &fa);
 }
 
 size_t query_sum_smem(const Geometry& g) {
@@ -748,12 +763,13 @@ cudaError_t launch_page_select(const Geometry& g, const float* summary, const in
   const size_t HD = (size_t)g.Hkv * g.d;
   char* w = (char*)ws;
   SelParams p;
-  p.n_new = 0;
-  if (job) {  // the caller has checked fused_append_ok
+  FusedAppend fa;
+  fa.n_new = 0;
+  if (job) {  // the caller has checked select_scores
     if (n_new <= 0 || n_new > kMaxFusedAppendPages) return cudaErrorInvalidValue;
-    p.n_new = n_new;
-    p.job = *job;
-    for (int i = 0; i < n_new; ++i) p.new_phys[i] = new_phys[i];
+    fa.n_new = n_new;
+    fa.job = *job;
+    for (int i = 0; i < n_new; ++i) fa.new_phys[i] = new_phys[i];
   }
   p.g = g;
   p.q = q;
@@ -790,7 +806,9 @@ cudaError_t launch_page_select(const Geometry& g, const float* summary, const in
   p.sum_off = 0;
 
   const bool bf16 = g.dtype != OOMB_FP32;
-  const void* fn = bf16 ? (const void*)page_select_kernel<__nv_bfloat16> : (const void*)page_select_kernel<float>;
+  const void* fn = job ? (bf16 ? (const void*)page_select_append_kernel<__nv_bfloat16>
+                               : (const void*)page_select_append_kernel<float>)
+                       : (bf16 ? (const void*)page_select_kernel<__nv_bfloat16> : (const void*)page_select_kernel<float>);
   if (!p.need_scores) {
     if (job) return cudaErrorInvalidValue;  // a fused append needs the cooperative grid
     void* args[] = {&p};
@@ -816,14 +834,14 @@ cudaError_t launch_page_select(const Geometry& g, const float* summary, const in
   if (p.keys_in_smem) smem = std::max(smem, align_up((size_t)p.n_cand, 4) * sizeof(uint32_t));
   if (smem > 200 * 1024) return cudaErrorInvalidValue;
   // the default dynamic limit is 48 KB minus the static shared memory: always opt in
-  static size_t smem_set[2][kMaxDevices] = {};
+  static size_t smem_set[2][2][kMaxDevices] = {};
   {
-    cudaError_t e = set_smem_limit(fn, smem, smem_set[bf16]);
+    cudaError_t e = set_smem_limit(fn, smem, smem_set[job ? 1 : 0][bf16]);
     if (e != cudaSuccess) return e;
   }
   // one CTA per SM always fits (<= 200 KB of shared memory, 512 threads); a grid that
   // could not be co-resident is refused by the cooperative launch itself
-  void* args[] = {&p};
+  void* args[] = {&p, &fa};
   cudaError_t e = cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(kThreads), args, smem, st);
   count_launches(1);
   return e;
