@@ -1187,33 +1187,38 @@ def main():
 
 
 class HostBuffer:
-    """One page-locked host allocation holding many tensors.  Plain pageable memory
-    registered with cudaHostRegister: exactly the bytes asked for (the caching pinned
-    allocator rounds each block up to a power of two, which would nearly double a
-    ~70 GB set of inputs), and async copies to and from it run at the link's speed."""
+    """Page-locked host memory for the end-to-end copies: blocks of exactly 1 GiB from
+    the pinned allocator (cudaHostAlloc; it rounds a request up to a power of two, so
+    such blocks waste nothing), the tensors packed into them, and a block of its own for
+    a tensor above 1 GiB.  Memory the driver allocates page-locked kept the copy rate
+    better than pageable memory registered with cudaHostRegister (1M tokens, fresh
+    machine: +0.2 % against +4.9 % end to end)."""
 
-    def __init__(self, nbytes: int):
-        import torch
-        self.buf = torch.empty(max(16, nbytes), dtype=torch.uint8)
-        self.off = 0
-        err = torch.cuda.cudart().cudaHostRegister(self.buf.data_ptr(), self.buf.numel(), 0)
-        if int(err) != 0:
-            raise RuntimeError(f"cudaHostRegister failed ({err})")
+    BLOCK = 1 << 30
+
+    def __init__(self):
+        self.blocks, self.cur, self.off = [], None, 0
 
     def take(self, shape, dtype):
         import torch
         n = int(math.prod(shape)) * torch.tensor([], dtype=dtype).element_size()
+        if n > self.BLOCK:
+            t = torch.empty(shape, dtype=dtype, pin_memory=True)
+            self.blocks.append(t)
+            return t
         self.off = (self.off + 255) // 256 * 256
-        t = self.buf[self.off:self.off + n].view(dtype).view(shape)
+        if self.cur is None or self.off + n > self.BLOCK:
+            self.cur = torch.empty(self.BLOCK, dtype=torch.uint8, pin_memory=True)
+            self.blocks.append(self.cur)
+            self.off = 0
+        t = self.cur[self.off:self.off + n].view(dtype).view(shape)
         self.off += n
         return t
 
     def close(self):
         import torch
-        if self.buf is not None:
-            torch.cuda.synchronize()
-            torch.cuda.cudart().cudaHostUnregister(self.buf.data_ptr())
-            self.buf = None
+        torch.cuda.synchronize()
+        self.blocks, self.cur = [], None
 
 
 E2E_AHEAD = 3  # chunks whose inputs are uploaded ahead of the forward sweep
@@ -1232,7 +1237,7 @@ def measure_e2e(step, steps, credited, world, dev):
     import torch
     sizes = [t.numel() * t.element_size() for ch in step.chunks for t in ch.values()]
     dq_sizes = [d.numel() * d.element_size() for d in step.dq]
-    hb = HostBuffer(sum(sizes) + sum(dq_sizes) + 256 * (len(sizes) + len(dq_sizes)))
+    hb = HostBuffer()
     host_in = [{k: hb.take(v.shape, v.dtype) for k, v in ch.items()} for ch in step.chunks]
     for ch, hc in zip(step.chunks, host_in):
         for k in ch:
@@ -1242,7 +1247,7 @@ def measure_e2e(step, steps, credited, world, dev):
     host_dk = host_dv = None
     w = step.w
     if pools_on_device:  # token-major dK, dV of the whole sequence; two device gather buffers
-        hp = HostBuffer(2 * w.seq * w.n_kv_heads * w.head_dim * 4 + 512)
+        hp = HostBuffer()
         host_dk = hp.take((w.seq, w.n_kv_heads, w.head_dim), torch.float32)
         host_dv = hp.take((w.seq, w.n_kv_heads, w.head_dim), torch.float32)
         gk = [torch.empty((w.chunk, w.n_kv_heads, w.head_dim), dtype=torch.float32, device=dev) for _ in range(2)]
