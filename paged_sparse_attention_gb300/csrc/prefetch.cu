@@ -10,12 +10,12 @@
 // stream instead of one copy call per block.
 //
 // Each launch is a small persistent grid (8 or 16 thread blocks of 256 threads,
-// at most 32 registers each) that walks the chunk's blocks: a block fits on an SM
-// beside an attention CTA (one per SM, 320-448 threads), so the transfers run while
-// the attention kernels hold the SMs (issue them on a high-priority stream, or the
-// block scheduler places them only after a long attention grid's last pending
-// block), and only a few SMs carry the long-latency host accesses, which slow the
-// other memory traffic of the SM they run on.
+// at most 32 registers each) that walks the chunk's blocks.  An attention CTA holds
+// nearly all of its SM's shared memory, so a transfer block takes an SM of its own
+// while it runs: issued on a high-priority stream (otherwise the block scheduler
+// places it only after a long attention grid's last pending block) it starts on the
+// next SM an attention CTA leaves, and a transfer takes only a few SMs from the
+// attention kernels.
 //
 //   gather_pages  K/V: slot (buf, h, s) <- pool block (phi(sel[h][s]), h), or the
 //                 reverse (to_host: a chunk's own pages appended into their slots only)
