@@ -72,6 +72,10 @@ def test_offload_pool_host_checks(lib):
     assert lib.oomb_prefetch_pages(pool, fake, fake, 8, 0, 3, 2, None) == 1
     assert lib.oomb_prefetch(pool, fake + 2, fake, 8, 0, None) == 3  # misaligned selection
     assert lib.oomb_kv_writeback(pool, fake, fake + 1, 8, 0, 0, 1, None) == 3
+    sa = lib.oomb_page_select_append
+    for mode in (1, 2):  # staged and deferred: the stage buffer and max_sel against the capacity
+        assert sa(pool, fake, fake, fake, 0, 128, 4, 1, fake, fake, 8, fake, 1 << 30, mode, 2, None) == 1
+        assert sa(pool, fake, fake, fake, 0, 128, 4, 1, fake, fake, 9, fake, 1 << 30, mode, 0, None) == 1
     assert lib.oomb_pool_free_pages(pool) == 4  # nothing was taken
     lib.oomb_pool_destroy(pool)
 
@@ -107,6 +111,16 @@ def test_allocator_host_logic(lib):
     assert lib.oomb_kv_writeback(pool, fake, fake, 8, 0, 2, 1, None) == 1  # end before start
     assert lib.oomb_kv_writeback(pool, None, fake, 8, 0, 0, 1, None) == 1
     assert lib.oomb_pool_set_stage(pool, 0) == 8
+    # the selection fused with the chunk's append: the append mode, the pool kind and
+    # the chunk's start (its K/V are appended by this call) are checked first
+    sa = lib.oomb_page_select_append
+    assert sa(pool, fake, fake, fake, 0, 128, 4, 1, fake, fake, 8, fake, 1 << 30, 3, 0, None) == 1
+    assert sa(pool, fake, fake, fake, 0, 128, 4, 1, fake, fake, 8, fake, 1 << 30, -1, 0, None) == 1
+    assert sa(pool, fake, fake, fake, 0, 128, 4, 1, fake, fake, 8, fake, 1 << 30, 1, 0, None) == 8
+    assert sa(pool, fake, fake, fake, 0, 128, 4, 1, fake, fake, 8, fake, 1 << 30, 2, 0, None) == 8
+    assert sa(pool, fake, fake, fake, 128, 128, 4, 1, fake, fake, 8, fake, 1 << 30, 0, 0, None) == 1
+    assert sa(None, fake, fake, fake, 0, 128, 4, 1, fake, fake, 8, fake, 1 << 30, 0, 0, None) == 1
+    assert lib.oomb_pool_free_pages(pool) == 4  # nothing was taken
     assert lib.oomb_workspace_size(pool, 0, 4096) > 0
     assert lib.oomb_workspace_size(pool, 1, 4096) >= 28 * 4096 * 4
     assert lib.oomb_workspace_size(pool, 9, 4096) == 0
