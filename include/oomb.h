@@ -419,7 +419,8 @@ OOMB_API oomb_status oomb_gemm(int m, int n, int k, int trans_a, int trans_b, co
  * which carries gradients back), or not at all (mode 0: bias and cast only).  bias:
  * fp32 [H*d] or NULL; in_dtype/out_dtype OOMB_BF16 or OOMB_FP32; in == out is allowed
  * for equal dtypes.  The angles' cos/sin are computed in double precision.
- * Errors: ARG (odd d, d > 128, theta <= 1 with a rotation), DTYPE, CUDA. */
+ * Errors: ARG (odd d, d > 128, theta <= 1 with a rotation), DTYPE, ALIGN (in, out or
+ * bias not on a multiple of its element size), CUDA. */
 OOMB_API oomb_status oomb_bias_rope(const void* in, int in_dtype, const float* bias, void* out, int out_dtype, int n,
                                     int H, int d, int64_t pos0, float theta, int mode, void* stream);
 

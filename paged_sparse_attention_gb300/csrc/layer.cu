@@ -208,6 +208,11 @@ oomb_status oomb_bias_rope(const void* in, int in_dtype, const float* bias, void
   if ((in_dtype != OOMB_BF16 && in_dtype != OOMB_FP32) || (out_dtype != OOMB_BF16 && out_dtype != OOMB_FP32))
     return OOMB_ERR_DTYPE;
   if (in == out && in_dtype != out_dtype) return OOMB_ERR_ARG;
+  // the kernel reads and writes single elements: each pointer on its element's size
+  const uintptr_t ea = in_dtype == OOMB_FP32 ? 4 : 2, eb = out_dtype == OOMB_FP32 ? 4 : 2;
+  if (reinterpret_cast<uintptr_t>(in) % ea || reinterpret_cast<uintptr_t>(out) % eb ||
+      reinterpret_cast<uintptr_t>(bias) % 4)
+    return OOMB_ERR_ALIGN;
   cudaStream_t st = (cudaStream_t)stream;
   cudaError_t e;
   if (in_dtype == OOMB_FP32 && out_dtype == OOMB_FP32)

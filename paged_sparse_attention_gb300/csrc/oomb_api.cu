@@ -161,6 +161,7 @@ oomb_status oomb_pool_create(const oomb_pool_desc* desc, oomb_pool** out) {
   const void* ptrs[] = {d.k_pool, d.v_pool, d.dk_pool, d.dv_pool, d.summary, d.error_word};
   for (const void* p : ptrs)
     if (!aligned(p, 16)) return OOMB_ERR_ALIGN;
+  if (!aligned(d.page_table, 4)) return OOMB_ERR_ALIGN;
   if (d.offload) {
     if (!d.stage_k || !d.stage_v || d.stage_max_sel <= 0) return OOMB_ERR_ARG;
     if (!aligned(d.stage_k, 16) || !aligned(d.stage_v, 16)) return OOMB_ERR_ALIGN;
@@ -575,6 +576,7 @@ oomb_status oomb_grad_prefetch(oomb_pool* p, const int32_t* sel, const int32_t* 
   oomb_status s = check_grad_call(p, sel, sel_count, max_sel, stage_buf);
   if (s != OOMB_OK) return s;
   if ((prev_sel == nullptr) != (prev_count == nullptr)) return OOMB_ERR_ARG;
+  if (!aligned(prev_sel, 4) || !aligned(prev_count, 4)) return OOMB_ERR_ALIGN;
   return cuda_status(launch_grad_copy(p->g, kGradFromHost, p->d.dk_pool, p->d.dv_pool, p->d.grad_state, p->d.page_table, sel,
                                       sel_count, prev_sel, prev_count, max_sel, p->d.stage_dk, p->d.stage_dv,
                                       stage_buf, p->d.stage_max_sel, p->d.error_word, (cudaStream_t)stream));
@@ -585,6 +587,7 @@ oomb_status oomb_grad_carry(oomb_pool* p, const int32_t* sel, const int32_t* sel
   oomb_status s = check_grad_call(p, sel, sel_count, max_sel, stage_buf);
   if (s != OOMB_OK) return s;
   if (!prev_sel || !prev_count) return OOMB_ERR_ARG;
+  if (!aligned(prev_sel, 4) || !aligned(prev_count, 4)) return OOMB_ERR_ALIGN;
   return cuda_status(launch_grad_copy(p->g, kGradCarry, p->d.dk_pool, p->d.dv_pool, p->d.grad_state, p->d.page_table, sel,
                                       sel_count, prev_sel, prev_count, max_sel, p->d.stage_dk, p->d.stage_dv,
                                       stage_buf, p->d.stage_max_sel, p->d.error_word, (cudaStream_t)stream));

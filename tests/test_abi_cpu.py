@@ -50,6 +50,7 @@ def test_pool_create_validation(lib):
     assert lib.oomb_pool_create(C.byref(_desc(head_dim=256)), C.byref(h)) == 8
     assert lib.oomb_pool_create(C.byref(_desc(k_pool=(1 << 20) + 4)), C.byref(h)) == 3
     assert lib.oomb_pool_create(C.byref(_desc(summary=None)), C.byref(h)) == 1
+    assert lib.oomb_pool_create(C.byref(_desc(page_table=(6 << 20) + 2)), C.byref(h)) == 3
     bad_order = (C.c_int32 * 4)(0, 1, 1, 2)
     assert lib.oomb_pool_create(C.byref(_desc(page_order=C.addressof(bad_order))), C.byref(h)) == 1
     assert lib.oomb_pool_create(C.byref(_desc(offload=1)), C.byref(h)) == 1  # no staging buffers
@@ -127,3 +128,46 @@ def test_allocator_host_logic(lib):
     tab = (C.c_int32 * 8)()
     assert lib.oomb_page_table_host(pool, tab, 8) == 8 and list(tab) == [-1] * 8
     lib.oomb_pool_destroy(pool)
+
+
+def test_gradient_transfer_host_checks(lib):
+    """An offload pool with host-resident gradient pools: the gradient stage-in, carry
+    and write-back check the stage buffer, the staging capacity and the alignment of
+    both selections (this chunk's and the previous chunk's) before any device work."""
+    h = C.c_void_p()
+    d = _desc(offload=1, offload_grads=1, stage_max_sel=8, stage_k=1 << 26, stage_v=1 << 27,
+              stage_dk=1 << 28, stage_dv=1 << 29, grad_state=1 << 30)
+    assert lib.oomb_pool_create(C.byref(d), C.byref(h)) == 0
+    pool = h.value
+    fake = 1 << 24
+    for fn in (lib.oomb_grad_prefetch, lib.oomb_grad_carry):
+        assert fn(pool, fake, fake, 8, fake, fake, 2, None) == 1        # stage buffer 2
+        assert fn(pool, fake, fake, 9, fake, fake, 0, None) == 1        # above the staging capacity
+        assert fn(pool, fake + 2, fake, 8, fake, fake, 0, None) == 3    # misaligned selection
+        assert fn(pool, fake, fake, 8, fake + 2, fake, 0, None) == 3    # misaligned previous selection
+        assert fn(pool, fake, fake, 8, fake, fake + 1, 0, None) == 3    # misaligned previous counts
+    assert lib.oomb_grad_prefetch(pool, fake, fake, 8, fake, None, 0, None) == 1  # one of the pair
+    assert lib.oomb_grad_carry(pool, fake, fake, 8, None, None, 0, None) == 1     # carry needs prev
+    assert lib.oomb_grad_writeback(pool, fake, fake, 8, 2, None) == 1
+    assert lib.oomb_grad_writeback(pool, fake, fake + 2, 8, 0, None) == 3
+    lib.oomb_pool_destroy(pool)
+    # without host-resident gradients the calls are unsupported
+    assert lib.oomb_pool_create(C.byref(_desc()), C.byref(h)) == 0
+    assert lib.oomb_grad_writeback(h.value, fake, fake, 8, 0, None) == 8
+    lib.oomb_pool_destroy(h.value)
+
+
+def test_rope_host_checks(lib):
+    """oomb_bias_rope refuses shapes it cannot run and pointers off their element size
+    before launching anything."""
+    fake = 1 << 24
+    bf16, fp32 = _lib.OOMB_BF16, _lib.OOMB_FP32
+    rope = lib.oomb_bias_rope
+    assert rope(fake, bf16, None, fake, bf16, 4, 2, 7, 0, 1e6, 1, None) == 1       # odd head dim
+    assert rope(fake, bf16, None, fake, bf16, 4, 2, 8, 0, 1.0, 1, None) == 1       # theta <= 1
+    assert rope(fake, 5, None, fake, bf16, 4, 2, 8, 0, 1e6, 1, None) == 4          # dtype
+    assert rope(fake, bf16, None, fake, fp32, 4, 2, 8, 0, 1e6, 1, None) == 1       # in place, two dtypes
+    assert rope(fake + 1, bf16, None, fake + 64, bf16, 4, 2, 8, 0, 1e6, 1, None) == 3
+    assert rope(fake + 2, fp32, None, fake + 64, fp32, 4, 2, 8, 0, 1e6, 1, None) == 3
+    assert rope(fake, bf16, fake + 2, fake + 64, bf16, 4, 2, 8, 0, 1e6, 1, None) == 3  # bias
+    assert rope(fake, bf16, None, fake + 65, bf16, 4, 2, 8, 0, 1e6, 1, None) == 3
